@@ -1,0 +1,205 @@
+/*
+ * coli_moe.h -- C ABI of libcolimoe, the routed Mixture-of-Experts layer of a
+ * GLM-5.2-style decoder on one sm_103a GPU.
+ *
+ * The layer (colibrì v1.0 README, "What's implemented"; "Colibri (colibrì):
+ * GLM-5.2 local inference on 25 GB of RAM", "How it works (validated core
+ * mechanics)"):
+ *   1. sigmoid noaux_tc router: s = sigmoid(x . Wr^T); experts ranked by
+ *      s + correction_bias inside the topk_group best groups; gate weights are
+ *      the unbiased s of the selection renormalised, times
+ *      routed_scaling_factor;
+ *   2. batch-union dispatch: each distinct expert of a call is streamed from
+ *      HBM once and applied to every position routed to it;
+ *   3. Q8_0-style int8 activations (blocks of 32, one fp32 scale each);
+ *   4. packed-int4 (or int8) x int8 SwiGLU expert products with per-row fp32
+ *      weight scales; h = silu(g) * u is re-quantised to Q8_0 before the down
+ *      product;
+ *   5. y = sum_j w_j * expert_j(x) + sum_s shared_s(x).
+ *
+ * Conventions for every entry point
+ *   - All tensor pointers are DEVICE pointers, row-major, owned by the caller;
+ *     the library allocates nothing and keeps no state between calls.
+ *   - Every pointer must be 16-byte aligned (TMA bulk copies read them).
+ *   - Work is enqueued on `stream`; no call synchronises except
+ *     coli_moe_status().  A call whose return value is not COLI_OK enqueued
+ *     nothing.
+ *   - Data-dependent failures (non-finite input, an out-of-range expert id,
+ *     an expired bounded wait) cannot be returned synchronously: they are OR-ed
+ *     into a sticky status word at the start of the workspace and read (and
+ *     cleared) with coli_moe_status().
+ *   - Calls that share a workspace must be ordered on one stream.
+ */
+#ifndef COLI_MOE_H
+#define COLI_MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Return codes (synchronous). */
+#define COLI_OK            0
+#define COLI_EINVAL       -1   /* bad shape, config or null pointer            */
+#define COLI_EALIGN       -2   /* a pointer is not 16-byte aligned             */
+#define COLI_EWORKSPACE   -3   /* workspace smaller than coli_moe_workspace_size */
+#define COLI_ECUDA        -4   /* a CUDA launch or query failed                */
+#define COLI_EUNSUPPORTED -5   /* shape outside the kernels' limits            */
+
+/* Device status bits (asynchronous, sticky until read by coli_moe_status). */
+#define COLI_STATUS_NONFINITE 1u  /* non-finite router logit, bias or activation */
+#define COLI_STATUS_BADIDX    2u  /* forward saw an expert id outside [-1, E)    */
+#define COLI_STATUS_TIMEOUT   4u  /* a bounded device wait expired               */
+
+/* Layer shape.  Limits: hidden % 32 == 0, inter % 32 == 0,
+ * shared_inter % 32 == 0, hidden % 64 == 0, n_experts <= 1024,
+ * n_experts % n_groups == 0, n_groups <= 32, 1 <= topk_group <= n_groups,
+ * 1 <= top_k <= topk_group * n_experts / n_groups, top_k <= 32,
+ * 0 <= n_shared <= 8, weight_bits in {4, 8}. */
+typedef struct coli_moe_cfg {
+    int32_t hidden;                 /* H                                    */
+    int32_t n_experts;              /* E routed experts                     */
+    int32_t n_groups;               /* G expert groups (E/G experts each)   */
+    int32_t topk_group;             /* groups kept per token                */
+    int32_t top_k;                  /* experts selected per token (k)       */
+    int32_t inter;                  /* I, intermediate size of routed experts */
+    int32_t n_shared;               /* always-on shared experts             */
+    int32_t shared_inter;           /* intermediate size of shared experts  */
+    int32_t weight_bits;            /* 4: packed int4, 8: int8              */
+    float   routed_scaling_factor;  /* multiplies the renormalised weights  */
+} coli_moe_cfg;
+
+/* Expert weights.  One expert "record" is its three matrices stored adjacent
+ * (colibrì "JustVugg/colibri" README, "Never wait for the disk twice": an
+ * expert's three matrices are read in one go):
+ *     gate [Ie][H], up [Ie][H], down [H][Ie]     (Ie = inter or shared_inter)
+ * each row-major with K (the reduction dimension) contiguous.
+ *   weight_bits 8: one int8 code per weight.
+ *   weight_bits 4: two codes per byte; byte j of a row holds element 2j in the
+ *                  low nibble and 2j+1 in the high nibble, each stored as
+ *                  code + 8 (codes in [-8, 7]).
+ * Records are consecutive: expert e starts at experts + e * record_bytes,
+ * record_bytes = (2*Ie*H + H*Ie) * weight_bits / 8.
+ * Scales are fp32 per output row, consecutive per expert:
+ *     expert_scales[e * (2*I + H) + {0..I-1: gate, I..2I-1: up, 2I..: down}]
+ * and likewise shared_scales with shared_inter. */
+typedef struct coli_moe_weights {
+    const void*  experts;        /* [n_experts] records                 */
+    const float* expert_scales;  /* [n_experts][2*inter + hidden]       */
+    const void*  shared;         /* [n_shared] records (shared_inter)   */
+    const float* shared_scales;  /* [n_shared][2*shared_inter + hidden] */
+} coli_moe_weights;
+
+/* Bytes of workspace needed for calls with up to max_T positions.  The
+ * workspace is caller-owned device memory; it must be prepared once with
+ * coli_moe_workspace_init() and may then be reused by any number of calls on
+ * one stream.  Returns 0 on an invalid config. */
+size_t coli_moe_workspace_size(const coli_moe_cfg* cfg, int32_t max_T);
+
+/* Clears the status word and the dispatch counters of a workspace
+ * (enqueued on `stream`). */
+int coli_moe_workspace_init(void* ws, size_t ws_bytes, cudaStream_t stream);
+
+/* Router: "How it works (validated core mechanics)" on the page-4 write-up
+ * (sigmoid affinities, bias for ranking only, lower id wins ties, unbiased
+ * renormalised weights, non-finite input rejected) with DeepSeek-V3 group
+ * limiting: group score = sum of the two best biased scores of the group,
+ * the topk_group best groups kept (ties to the lower group id), dropped
+ * groups never selectable.
+ *   x          [T][H]  fp32 activations
+ *   router_w   [E][H]  fp32 router weight
+ *   corr_bias  [E]     fp32 correction bias (ranking only)
+ *   topk_idx   [T][k]  int32 out: expert ids by descending biased score
+ *   topk_w     [T][k]  fp32  out: s_sel / sum(s_sel) * routed_scaling_factor
+ * Logits are fp32.  A position with a non-finite logit or bias gets ids -1
+ * and weights 0, and sets COLI_STATUS_NONFINITE.  T == 0 is a no-op. */
+int coli_moe_route(const coli_moe_cfg* cfg, const float* x, int32_t T,
+                   const float* router_w, const float* corr_bias,
+                   int32_t* topk_idx, float* topk_w,
+                   void* ws, size_t ws_bytes, cudaStream_t stream);
+
+/* Q8_0-style activation quantisation (colibrì v1.0 README, "What's
+ * implemented", integer-dot kernels): per block of 32 consecutive values,
+ * d = amax/127 (IEEE fp32), inv = d > 0 ? 1/d : 0,
+ * q = clamp(roundf(x * inv), -127, 127) (half away from zero).
+ *   x [T][K] fp32 in, K % 32 == 0;  q [T][K] int8 out;  d [T][K/32] fp32 out.
+ * A non-finite value gives code 0 for its element (no status word: this
+ * entry point takes no workspace). */
+int coli_moe_quantize_act(const float* x, int32_t T, int32_t K,
+                          int8_t* q, float* d, cudaStream_t stream);
+
+/* The expert layer for given routing: quantise x, build the batch-union
+ * tables, run each distinct expert once over its positions (gate/up, SwiGLU,
+ * re-quantise h, down) and combine
+ *     y[t] = sum_j topk_w[t][j] * o[t,j] + sum_s o_shared_s[t]
+ * in fixed j order (deterministic, no floating-point atomics).
+ *   x        [T][H] fp32;   topk_idx [T][k] int32 (id -1: slot skipped);
+ *   topk_w   [T][k] fp32;   y [T][H] fp32 out.
+ * Ids outside [-1, E) are skipped and set COLI_STATUS_BADIDX; non-finite
+ * activations set COLI_STATUS_NONFINITE.  T == 0 is a no-op. */
+int coli_moe_forward(const coli_moe_cfg* cfg, const coli_moe_weights* weights,
+                     const float* x, int32_t T,
+                     const int32_t* topk_idx, const float* topk_w, float* y,
+                     void* ws, size_t ws_bytes, cudaStream_t stream);
+
+/* The two launches coli_moe_forward makes, callable separately (e.g. to time
+ * the expert kernel alone).  coli_moe_dispatch quantises x and builds the
+ * union tables in ws; coli_moe_experts runs the expert products and the
+ * combine from those tables.  Same arguments and rules as coli_moe_forward;
+ * coli_moe_experts must follow a coli_moe_dispatch with the same T on the
+ * same workspace. */
+int coli_moe_dispatch(const coli_moe_cfg* cfg, const float* x, int32_t T,
+                      const int32_t* topk_idx, void* ws, size_t ws_bytes,
+                      cudaStream_t stream);
+int coli_moe_experts(const coli_moe_cfg* cfg, const coli_moe_weights* weights,
+                     int32_t T, const float* topk_w, float* y,
+                     void* ws, size_t ws_bytes, cudaStream_t stream);
+
+/* Synchronises `stream`, returns the workspace's status bits in *status and
+ * clears them. */
+int coli_moe_status(void* ws, cudaStream_t stream, uint32_t* status);
+
+/* Static text for a return code. */
+const char* coli_moe_strerror(int code);
+
+/* ---- inspection (tests) -------------------------------------------------
+ * Byte offsets, inside the workspace of coli_moe_workspace_size(cfg, max_T),
+ * of the tables and intermediates coli_moe_dispatch / coli_moe_experts leave
+ * behind, so that a test can compare them with a reference.  Layouts:
+ *   n_entries   int32: routed distinct experts U + n_shared
+ *   entry_expert[U+n_shared] int32: ascending routed ids, then E + s
+ *   entry_count [U+n_shared] int32: positions per entry
+ *   entry_offset[U+n_shared+1] int32: first pair slot of each entry
+ *   pair_token  [P] int32, pair_slot_of[T][k] int32 (-1 = skipped)
+ *   qx [T][H] int8, dx [T][H/32] fp32  (Q8_0 of x)
+ *   qh [P][Imax] int8, dh [P][Imax/32] fp32 (Q8_0 of h per pair slot)
+ *   o  [P][H] fp32 (expert output per pair slot)
+ * with P = T*k + n_shared*T and Imax = max(inter, shared_inter).  For
+ * weight_bits 4, qx and qh hold each group of 8 consecutive codes in the
+ * order 0,2,4,6,1,3,5,7 (the order of the low then high nibbles of 4 packed
+ * bytes); for weight_bits 8 the order is natural. */
+typedef struct coli_moe_ws_layout {
+    size_t status, n_entries, entry_expert, entry_count, entry_offset,
+           pair_token, pair_slot_of, qx, dx, qh, dh, o, total;
+} coli_moe_ws_layout;
+int coli_moe_workspace_layout(const coli_moe_cfg* cfg, int32_t max_T,
+                              coli_moe_ws_layout* out);
+
+/* Test entry point: coli_moe_forward run through the same kernels compiled
+ * with a dump of the exact int32 per-32-block dot products:
+ *   acc_gu [P][2][Imax][H/32] int32   (gate then up, per pair slot)
+ *   acc_d  [P][H][Imax/32]    int32   (down, per pair slot)
+ * Either pointer may be NULL.  Slower than coli_moe_forward. */
+int coli_moe_forward_dump(const coli_moe_cfg* cfg, const coli_moe_weights* weights,
+                          const float* x, int32_t T,
+                          const int32_t* topk_idx, const float* topk_w, float* y,
+                          void* ws, size_t ws_bytes,
+                          int32_t* acc_gu, int32_t* acc_d, cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* COLI_MOE_H */

@@ -1,0 +1,207 @@
+// Router kernels: fp32 logits x . Wr^T, then the sigmoid noaux_tc group
+// top-k selection ("Colibri (colibrì): GLM-5.2 local inference on 25 GB of
+// RAM", "How it works (validated core mechanics)"; DeepSeek-V3 group
+// limiting as named on that page).
+#include "colimoe_internal.cuh"
+
+namespace colimoe {
+
+// Logits for T <= 8 positions: one warp per (expert, K split), lanes stride
+// float4 columns, partial sums to part[split][t][e] (summed in fixed order by
+// the selection kernel, so results do not depend on scheduling).
+__global__ void __launch_bounds__(256) route_logits_gemv(const float* __restrict__ x, int T, int H,
+                                                         const float* __restrict__ wr, int E,
+                                                         int splits, float* __restrict__ part) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int e = blockIdx.x * 8 + warp;
+  const int s = blockIdx.y;
+  if (e >= E) return;
+  const int n4 = H / 4 / splits;
+  const float4* w4 = reinterpret_cast<const float4*>(wr + (size_t)e * H) + (size_t)s * n4;
+  float acc[ROUTE_GEMV_MAX_T];
+#pragma unroll
+  for (int t = 0; t < ROUTE_GEMV_MAX_T; ++t) acc[t] = 0.f;
+#pragma unroll 6
+  for (int i = lane; i < n4; i += 32) {
+    float4 w = __ldg(w4 + i);
+#pragma unroll
+    for (int t = 0; t < ROUTE_GEMV_MAX_T; ++t) {
+      if (t < T) {
+        float4 v = __ldg(reinterpret_cast<const float4*>(x + (size_t)t * H) + (size_t)s * n4 + i);
+        acc[t] = fmaf(w.x, v.x, acc[t]);
+        acc[t] = fmaf(w.y, v.y, acc[t]);
+        acc[t] = fmaf(w.z, v.z, acc[t]);
+        acc[t] = fmaf(w.w, v.w, acc[t]);
+      }
+    }
+  }
+#pragma unroll
+  for (int t = 0; t < ROUTE_GEMV_MAX_T; ++t) {
+    if (t < T) {
+      float v = warp_sum(acc[t]);
+      if (lane == 0) part[((size_t)s * T + t) * E + e] = v;
+    }
+  }
+}
+
+// Logits for larger T: 64x64 output tiles, K steps of 16, 4x4 per thread.
+__global__ void __launch_bounds__(256) route_logits_tiled(const float* __restrict__ x, int T, int H,
+                                                          const float* __restrict__ wr, int E,
+                                                          float* __restrict__ part) {
+  __shared__ float xs[16][64 + 4];
+  __shared__ float ws[16][64 + 4];
+  const int t0 = blockIdx.y * 64, e0 = blockIdx.x * 64;
+  const int tid = threadIdx.x;
+  const int ty = tid / 16, tx = tid % 16;
+  float acc[4][4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
+  // loader: row = tid / 4 (0..63), k4 = tid % 4 (float4 index within 16)
+  const int lr = tid / 4, lk = (tid % 4) * 4;
+  for (int k0 = 0; k0 < H; k0 += 16) {
+    float4 xv = make_float4(0.f, 0.f, 0.f, 0.f), wv = xv;
+    if (t0 + lr < T) xv = __ldg(reinterpret_cast<const float4*>(x + (size_t)(t0 + lr) * H + k0 + lk));
+    if (e0 + lr < E) wv = __ldg(reinterpret_cast<const float4*>(wr + (size_t)(e0 + lr) * H + k0 + lk));
+    xs[lk + 0][lr] = xv.x; xs[lk + 1][lr] = xv.y; xs[lk + 2][lr] = xv.z; xs[lk + 3][lr] = xv.w;
+    ws[lk + 0][lr] = wv.x; ws[lk + 1][lr] = wv.y; ws[lk + 2][lr] = wv.z; ws[lk + 3][lr] = wv.w;
+    __syncthreads();
+#pragma unroll
+    for (int kk = 0; kk < 16; ++kk) {
+      float a[4], b[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) a[i] = xs[kk][ty * 4 + i];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) b[j] = ws[kk][tx * 4 + j];
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+    }
+    __syncthreads();
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int t = t0 + ty * 4 + i;
+    if (t >= T) continue;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int e = e0 + tx * 4 + j;
+      if (e < E) part[(size_t)t * E + e] = acc[i][j];
+    }
+  }
+}
+
+struct ArgMax { float v; int i; };
+__device__ __forceinline__ ArgMax better(ArgMax a, ArgMax b) {
+  // larger value wins, equal values go to the lower index
+  return (b.v > a.v || (b.v == a.v && b.i < a.i)) ? b : a;
+}
+__device__ __forceinline__ ArgMax warp_argmax(ArgMax a) {
+#pragma unroll
+  for (int o = 16; o; o >>= 1) {
+    ArgMax b{__shfl_xor_sync(0xffffffffu, a.v, o), __shfl_xor_sync(0xffffffffu, a.i, o)};
+    a = better(a, b);
+  }
+  return a;
+}
+
+// One warp per position: sigmoid, biased ranking score, group scores (sum
+// of the two best scores of each group), keep topk_group groups, top-k among
+// their experts (descending score, lower id on ties), weights from the
+// unbiased affinities renormalised and scaled.
+__global__ void __launch_bounds__(256) route_select(const float* __restrict__ part, int splits, int T,
+                                                   int E, int G, int topk_group, int k, float rsf,
+                                                   const float* __restrict__ bias,
+                                                   int32_t* __restrict__ topk_idx,
+                                                   float* __restrict__ topk_w,
+                                                   uint32_t* __restrict__ status) {
+  extern __shared__ float sm_sel[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t = blockIdx.x * 8 + warp;
+  if (t >= T) return;
+  float* s_aff = sm_sel + (size_t)warp * 2 * E;
+  float* s_c = s_aff + E;
+  bool bad = false;
+  for (int e = lane; e < E; e += 32) {
+    float l = 0.f;
+    for (int s = 0; s < splits; ++s) l += part[((size_t)s * T + t) * E + e];
+    float b = bias[e];
+    if (!isfinite(l) || !isfinite(b)) bad = true;
+    float sv = __fdiv_rn(1.0f, 1.0f + expf(-l));
+    s_aff[e] = sv;
+    s_c[e] = sv + b;
+  }
+  if (__any_sync(0xffffffffu, bad)) {
+    if (lane == 0) atomicOr(status, COLI_STATUS_NONFINITE);
+    if (lane < k) {
+      topk_idx[(size_t)t * k + lane] = -1;
+      topk_w[(size_t)t * k + lane] = 0.f;
+    }
+    return;
+  }
+  __syncwarp();
+  const int gsz = E / G;
+  float gscore = -INFINITY;
+  if (lane < G) {
+    float b1 = -INFINITY, b2 = -INFINITY;
+    for (int i = 0; i < gsz; ++i) {
+      float v = s_c[lane * gsz + i];
+      if (v > b1) { b2 = b1; b1 = v; } else if (v > b2) { b2 = v; }
+    }
+    gscore = gsz >= 2 ? b1 + b2 : b1;
+  }
+  bool kept = false;
+  for (int r = 0; r < topk_group; ++r) {
+    ArgMax a{(lane < G && !kept) ? gscore : -INFINITY, lane < G ? lane : 1 << 20};
+    a = warp_argmax(a);
+    if (lane == a.i) kept = true;
+  }
+  const unsigned keptmask = __ballot_sync(0xffffffffu, kept);
+  int my_sel = -1;
+  for (int r = 0; r < k; ++r) {
+    ArgMax best{-INFINITY, 1 << 20};
+    for (int e = lane; e < E; e += 32) {
+      if (!((keptmask >> (e / gsz)) & 1u)) continue;
+      float v = s_c[e];
+      if (v == -INFINITY) continue;  // already selected
+      best = better(best, ArgMax{v, e});
+    }
+    best = warp_argmax(best);
+    if (lane == r) my_sel = best.i;
+    if (best.i < E && lane == (best.i & 31)) s_c[best.i] = -INFINITY;
+    __syncwarp();
+  }
+  float my_s = (lane < k && my_sel >= 0 && my_sel < E) ? s_aff[my_sel] : 0.f;
+  float tot = warp_sum(my_s);
+  if (lane < k) {
+    topk_idx[(size_t)t * k + lane] = my_sel;
+    topk_w[(size_t)t * k + lane] = tot > 0.f ? __fmul_rn(__fdiv_rn(my_s, tot), rsf) : 0.f;
+  }
+}
+
+cudaError_t launch_route(const float* x, int T, int H, const float* wr, int E, int G, int topk_group, int k,
+                         float rsf, const float* bias, int32_t* topk_idx, float* topk_w, float* part,
+                         uint32_t* status, cudaStream_t st) {
+  int splits = 1;
+  if (T <= ROUTE_GEMV_MAX_T) {
+    splits = GEMV_SPLITS;
+    while (splits > 1 && (H / 4) % (splits * 32)) splits /= 2;
+    dim3 grid((E + 7) / 8, splits);
+    route_logits_gemv<<<grid, 256, 0, st>>>(x, T, H, wr, E, splits, part);
+  } else {
+    dim3 grid((E + 63) / 64, (T + 63) / 64);
+    route_logits_tiled<<<grid, 256, 0, st>>>(x, T, H, wr, E, part);
+  }
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const size_t smem = (size_t)8 * 2 * E * sizeof(float);
+  e = cudaFuncSetAttribute(route_select, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  route_select<<<(T + 7) / 8, 256, smem, st>>>(part, splits, T, E, G, topk_group, k, rsf, bias, topk_idx,
+                                               topk_w, status);
+  return cudaGetLastError();
+}
+
+}  // namespace colimoe

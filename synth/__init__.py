@@ -250,6 +250,14 @@ def router_bias(shape: LayerShape, seed, layer=0):
     return uniform_f32(key, shape.n_experts, BIAS_LO, BIAS_HI)
 
 
+def zero_router_bias(shape: LayerShape):
+    """Correction bias of the uniform-routing (prefill) workload: with every
+    expert's bias equal the experts are exchangeable, so positions spread
+    uniformly over them (a U(-0.1, 0.1) bias dominates the ranking once the
+    selected sigmoid scores saturate near 1 and starves some experts)."""
+    return np.zeros(shape.n_experts, np.float32)
+
+
 def zipf_router_bias(shape: LayerShape, seed, layer, s=1.1, amp=0.3):
     """Correction bias skewed by a Zipf(s) profile over a seeded permutation."""
     base = router_bias(shape, seed, layer).astype(np.float64)
@@ -317,3 +325,14 @@ def mtp_chain(shape: LayerShape, seed, call, n_pos=4, attempts=None):
         z = token_x(shape, seed, ("mtp", call), p, a[p]).astype(np.float64)
         rows.append(rho * rows[-1] + math.sqrt(1.0 - rho * rho) * z)
     return np.stack(rows).astype(np.float32)
+
+
+def stack_input(shape: LayerShape, seed, step, layer, batch=32):
+    """Input of layer ``layer`` at decode step ``step`` of the layer stack:
+    x_0 ~ N(0,1) per sequence, then x_{l+1} = x_l + delta_l with a seeded
+    residual delta_l ~ N(0, 0.1^2) (fp32 adds, in layer order).  The layer
+    outputs are not fed back, so every layer's input is known in advance."""
+    x = token_batch(shape, seed, ("stack", step), range(batch))
+    for l in range(layer):
+        x = (x + residual_delta(shape, seed, step, l)[:batch * shape.hidden].reshape(batch, -1)).astype(np.float32)
+    return x

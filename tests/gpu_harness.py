@@ -1,0 +1,199 @@
+"""GPU-side harness for the parity tests: builds a layer on the device, runs
+the library through its C ABI and compares every observable with the oracle.
+Imported only by tests marked ``gpu``."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle
+import synth
+import quantized_expert_ffn_sigmoid_gb300 as cm
+from helpers import normwise_err, unpermute_int4
+
+Y_TOL = 1e-3     # max normwise relative error of the layer output
+W_RTOL = 1e-5    # gate weights: fp32 router vs fp64 oracle
+
+
+class DeviceLayer:
+    """One MoE layer's weights on the GPU plus lazily copied host views."""
+
+    def __init__(self, shape, seed, layer=0, device_weights=False, bias="uniform", dev="cuda"):
+        self.shape, self.seed, self.layer, self.dev = shape, seed, layer, dev
+        self.cfg = cm.Cfg.of(shape)
+        if device_weights:
+            import synth.gpu as sg
+            self.recs, self.scs = sg.expert_records(shape, seed, layer, "routed", shape.n_experts, dev)
+            if shape.n_shared:
+                self.srec, self.ssc = sg.expert_records(shape, seed, layer, "shared", shape.n_shared, dev)
+            else:
+                self.srec = self.ssc = None
+            self._host = {}
+        else:
+            routed = [synth.expert_record(shape, seed, layer, "routed", e) for e in range(shape.n_experts)]
+            shared = [synth.expert_record(shape, seed, layer, "shared", s) for s in range(shape.n_shared)]
+            self._host = {("routed", e): r for e, r in enumerate(routed)}
+            self._host.update({("shared", s): r for s, r in enumerate(shared)})
+            t = lambda a: torch.from_numpy(np.ascontiguousarray(np.stack(a))).to(dev)
+            self.recs, self.scs = t([r for r, _ in routed]), t([s for _, s in routed])
+            if shared:
+                self.srec, self.ssc = t([r for r, _ in shared]), t([s for _, s in shared])
+            else:
+                self.srec = self.ssc = None
+        self.W = cm.make_weights(self.recs, self.scs, self.srec, self.ssc)
+        self.router_w = synth.router_weight(shape, seed, layer)
+        self.bias = {"uniform": lambda: synth.router_bias(shape, seed, layer),
+                     "zipf": lambda: synth.zipf_router_bias(shape, seed, layer),
+                     "zero": lambda: synth.zero_router_bias(shape)}[bias]()
+        self.wr_d = torch.from_numpy(self.router_w).to(dev)
+        self.bias_d = torch.from_numpy(self.bias).to(dev)
+
+    def get_record(self, kind, e):
+        key = (kind, int(e))
+        if key not in self._host:
+            if kind == "routed":
+                self._host[key] = (self.recs[e].cpu().numpy(), self.scs[e].cpu().numpy())
+            else:
+                self._host[key] = (self.srec[e].cpu().numpy(), self.ssc[e].cpu().numpy())
+        return self._host[key]
+
+    # ------------------------------------------------------------------ runs
+    def run(self, x: np.ndarray, dump=True, ws=None, route=True, idx=None, w=None):
+        """Route (unless idx/w given) and forward; returns the GPU observables."""
+        shape, dev = self.shape, self.dev
+        T, k = x.shape[0], shape.top_k
+        xd = torch.from_numpy(np.ascontiguousarray(x, np.float32)).to(dev)
+        if ws is None:
+            ws = cm.new_workspace(self.cfg, T)
+        if route:
+            idx_d = torch.full((T, k), -7, dtype=torch.int32, device=dev)
+            w_d = torch.full((T, k), -7.0, dtype=torch.float32, device=dev)
+            cm.coli_moe_route(self.cfg, xd, self.wr_d, self.bias_d, idx_d, w_d, ws)
+        else:
+            idx_d = torch.from_numpy(np.ascontiguousarray(idx, np.int32)).to(dev)
+            w_d = torch.from_numpy(np.ascontiguousarray(w, np.float32)).to(dev)
+        y = torch.full((T, shape.hidden), float("nan"), dtype=torch.float32, device=dev)
+        L = cm.coli_moe_workspace_layout(self.cfg, T)
+        P = T * k + shape.n_shared * T
+        imax = max(shape.inter, shape.shared_inter if shape.n_shared else 0)
+        acc_gu = acc_d = None
+        if dump:
+            acc_gu = torch.zeros((P, 2, imax, shape.hidden // 32), dtype=torch.int32, device=dev)
+            acc_d = torch.zeros((P, shape.hidden, imax // 32), dtype=torch.int32, device=dev)
+            cm.coli_moe_forward_dump(self.cfg, self.W, xd, idx_d, w_d, y, ws, acc_gu, acc_d)
+        else:
+            cm.coli_moe_forward(self.cfg, self.W, xd, idx_d, w_d, y, ws)
+        status = cm.coli_moe_status(ws)
+        wsh = ws.cpu().numpy()
+
+        def view(off, dtype, count):
+            return np.frombuffer(wsh[off:off + np.dtype(dtype).itemsize * count].tobytes(), dtype)
+
+        n_ent = int(view(L.n_entries, np.int32, 1)[0])
+        out = dict(idx=idx_d.cpu().numpy(), w=w_d.cpu().numpy(), y=y.cpu().numpy(), status=status,
+                   n_entries=n_ent,
+                   entry_expert=view(L.entry_expert, np.int32, n_ent),
+                   entry_count=view(L.entry_count, np.int32, n_ent),
+                   entry_offset=view(L.entry_offset, np.int32, n_ent + 1),
+                   pair_token=view(L.pair_token, np.int32, P),
+                   slot=view(L.pair_slot_of, np.int32, T * k).reshape(T, k))
+        qx = view(L.qx, np.int8, T * shape.hidden).reshape(T, shape.hidden)
+        qh = view(L.qh, np.int8, P * imax).reshape(P, imax)
+        if shape.weight_bits == 4:
+            qx, qh = unpermute_int4(qx), unpermute_int4(qh)
+        out.update(qx=qx, dx=view(L.dx, np.float32, T * shape.hidden // 32).reshape(T, -1),
+                   qh=qh, dh=view(L.dh, np.float32, P * imax // 32).reshape(P, -1))
+        if dump:
+            out.update(acc_gu=acc_gu.cpu().numpy(), acc_d=acc_d.cpu().numpy())
+        return out
+
+
+def check_parity(layer: DeviceLayer, x, g, ref=None, idx=None, w=None, tokens=None):
+    """Compare GPU observables ``g`` with the oracle.  ``tokens`` restricts the
+    expert-level comparisons (and y) to a sample of positions."""
+    shape = layer.shape
+    T = x.shape[0]
+    assert g["status"] == 0, f"device status {g['status']}"
+    if idx is None:
+        logits = oracle.router_logits(x, layer.router_w)
+        ridx, rw = oracle.route(logits, layer.bias, shape)
+        assert np.array_equal(g["idx"], ridx), "routing indices differ"
+        np.testing.assert_allclose(g["w"], rw, rtol=W_RTOL, atol=1e-7)
+        idx, w = ridx, rw            # the oracle runs on its own routing
+    tabs = oracle.union_tables(idx, shape.n_experts, shape.n_shared)
+    n_ent = tabs["counts"].size
+    assert g["n_entries"] == n_ent
+    exp_ids = np.concatenate([tabs["uniq"], shape.n_experts + np.arange(shape.n_shared)])
+    assert np.array_equal(g["entry_expert"], exp_ids)
+    assert np.array_equal(g["entry_count"], tabs["counts"])
+    assert np.array_equal(g["entry_offset"], tabs["offsets"])
+    npair = int(tabs["offsets"][-1])
+    assert np.array_equal(g["pair_token"][:npair], tabs["pair_token"])
+    assert np.array_equal(g["slot"], tabs["slot"])
+    qx, dx = oracle.q8_0_quantize(x.astype(np.float32))
+    assert np.array_equal(g["qx"], qx), "Q8_0 codes of x differ"
+    assert np.array_equal(g["dx"], dx), "Q8_0 scales of x differ"
+
+    sel = np.arange(T) if tokens is None else np.asarray(tokens)
+    ref = oracle.moe_forward(shape, layer.get_record, x[sel], idx[sel], w[sel], keep_pairs=True)
+    # map oracle pairs of the sampled positions onto GPU pair slots
+    stats = dict(qh_checked=0, qh_unstable=0, qh_flips=0, accd_blocks=0)
+    for (kind, e), pr in ref["pairs"].items():
+        inter = shape.inter if kind == "routed" else shape.shared_inter
+        for n, tl in enumerate(pr["tokens"]):
+            t = int(sel[tl])
+            if kind == "routed":
+                p = int(g["slot"][t, pr["js"][n]])
+            else:
+                p = int(tabs["offsets"][tabs["uniq"].size + e] + t)
+            if "acc_gu" in g:
+                assert np.array_equal(g["acc_gu"][p, 0, :inter], pr["acc_g"][n]), "gate block dots differ"
+                assert np.array_equal(g["acc_gu"][p, 1, :inter], pr["acc_u"][n]), "up block dots differ"
+            qh_g = g["qh"][p, :inter].astype(np.int64)
+            qh_r = pr["qh"][n].astype(np.int64)
+            st = pr["qh_stable"][n]
+            assert np.array_equal(qh_g[st], qh_r[st]), "requantised h differs where unique"
+            assert np.abs(qh_g - qh_r).max(initial=0) <= 1
+            stats["qh_checked"] += qh_g.size
+            stats["qh_unstable"] += int((~st).sum())
+            stats["qh_flips"] += int((qh_g != qh_r).sum())
+            # block scale: amax/127 of h, within the h error bound of the oracle
+            dh_tol = 4.0 * pr["h_err"][n].reshape(-1, 32).max(axis=1) / 127.0 \
+                + np.abs(pr["dh"][n]).astype(np.float64) * 2.0 ** -21
+            assert np.all(np.abs(g["dh"][p, :inter // 32].astype(np.float64) - pr["dh"][n]) <= dh_tol)
+            if "acc_d" in g:
+                blk_ok = st.reshape(-1, 32).all(axis=1)
+                ad = g["acc_d"][p, :, :inter // 32]
+                assert np.array_equal(ad[:, blk_ok], pr["acc_d"][n][:, blk_ok]), "down block dots differ"
+                stats["accd_blocks"] += int(blk_ok.sum())
+    err = normwise_err(g["y"][sel], ref["y"])
+    assert err <= Y_TOL, f"layer output error {err:.3e}"
+    stats["y_err"] = err
+    # elementwise: fp32 evaluation bound plus the effect of every +-1 flip of
+    # a requantised h code the GPU took at a non-unique position
+    bound = np.zeros_like(ref["y"])
+    for (kind, e), pr in ref["pairs"].items():
+        inter = shape.inter if kind == "routed" else shape.shared_inter
+        rec, sc = layer.get_record(kind, e)
+        wd = oracle.unpack_weight_rows(np.asarray(rec).reshape(-1)[2 * inter * shape.row_bytes(shape.hidden):],
+                                       shape.hidden, inter, shape.weight_bits).astype(np.float64)
+        s_d = np.asarray(sc, np.float64)[2 * inter:2 * inter + shape.hidden]
+        for n, tl in enumerate(pr["tokens"]):
+            t = int(sel[tl])
+            if kind == "routed":
+                p = int(g["slot"][t, pr["js"][n]])
+                wt = abs(float(w[t, pr["js"][n]]))
+            else:
+                p = int(tabs["offsets"][tabs["uniq"].size + e] + t)
+                wt = 1.0
+            dh = pr["dh"][n].astype(np.float64)
+            ddh = 4.0 * pr["h_err"][n].reshape(-1, 32).max(axis=1) / 127.0 + dh * 2.0 ** -21
+            acc = np.abs(pr["acc_d"][n]).astype(np.float64)
+            dq = np.abs(g["qh"][p, :inter].astype(np.int64) - pr["qh"][n]).astype(np.float64)
+            flip = (np.abs(wd) * (dq * np.repeat(dh + ddh, 32))[None, :]).sum(axis=1)
+            term = 4.0 * pr["o_err"][n] + s_d * (acc @ ddh) + s_d * flip
+            # combine rounding (fp32, k + n_shared terms) and fp32 gate weights
+            bound[tl] += wt * (term + np.abs(pr["o"][n]) * (2.0 ** -20 + 2e-6))
+    dy = np.abs(g["y"][sel].astype(np.float64) - ref["y"])
+    assert np.all(dy <= bound + 1e-30), f"elementwise output bound exceeded by {(dy - bound).max():.3e}"
+    return stats
