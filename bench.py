@@ -1,0 +1,532 @@
+"""Throughput of the routed-MoE layer on GB300 (one JSON line on stdout).
+
+Headline workload: the GLM-5.2-shaped MoE layer at decode batch 1 (hidden
+6144, 256 routed experts in 8 groups, topk_group 4, top-8, moe_inter 2048,
+one shared expert, packed int4 per-row-scaled weights, all experts resident
+in HBM); one step = 1000 independent seeded positions, one layer call each
+(router + expert layer through the C ABI), back to back.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+* value: tokens/s with inputs resident in HBM, timed with CUDA events around
+  K steps replayed from a CUDA graph; L2 is defeated by rotating 8 identical
+  copies of the layer's weights (≈39 GB), so consecutive calls never find a
+  weight byte in L2.
+* roofline: the expert kernel's algorithmic bytes per launch (9 expert
+  records: 8 routed + the shared one) over its average launch duration,
+  measured with CUDA events on its stream, against the measured HBM copy
+  bandwidth.
+* e2e: the same tokens/s through the public API called per position from
+  Python with host buffers: pinned x copied in, y copied out, inside the timed
+  region.
+* cpu_baseline / --impl reference: the CPU oracle (numpy, one thread) timed on
+  a bounded sample of the same workload.
+Multi-GPU (torchrun): every rank runs its own 1000 positions on its own copy
+of the layer (weak scaling, no collective on the data path).
+"""
+from __future__ import annotations
+
+import os
+
+os.environ.setdefault("OPENBLAS_NUM_THREADS", "1")  # the CPU oracle runs on one thread
+os.environ.setdefault("OMP_NUM_THREADS", "1")
+
+import argparse  # noqa: E402
+import json  # noqa: E402
+import statistics  # noqa: E402
+import subprocess  # noqa: E402
+import sys  # noqa: E402
+import time  # noqa: E402
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import synth  # noqa: E402
+
+METRIC = "routed-MoE layer tokens/s + achieved HBM GB/s (decode) / int8 TOPS (prefill)"
+UNIT = "tokens/s"
+EXPERT_BYTES = synth.GLM.record_bytes() + 4 * synth.GLM.scale_count()   # 18,915,328
+ROUTER_BYTES = 4 * synth.GLM.n_experts * synth.GLM.hidden + 4 * synth.GLM.n_experts
+DECODE_TOKENS = 1000
+REPLICAS = 8
+WORKLOAD = ("glm_decode_b1: GLM-5.2-shaped MoE layer (H 6144, E 256 in 8 groups, topk_group 4, top-8, "
+            "moe_inter 2048, 1 shared expert, int4 per-row scales, rsf 2.5), decode batch 1, "
+            "1000 independent seeded positions per step, one layer call each")
+
+
+def log(*a):
+    print(*a, file=sys.stderr, flush=True)
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def max_over_ranks(value: float, world: int, device=None) -> float:
+    """Max of a per-rank float over all ranks (identity for one rank)."""
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(value: float, world: int, device=None) -> float:
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+def read_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p.get("bf16_tflops", 1937.1)), "measured"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, 1900.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons; only samples taken
+    between mark_start() and mark_end() are summarised."""
+    Q = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.t0 = self.t1 = None
+        self.out = ""
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def mark_start(self):
+        self.t0 = time.time()
+
+    def mark_end(self):
+        self.t1 = time.time()
+
+    def __exit__(self, *exc):
+        if self.proc is None:
+            return
+        time.sleep(0.1)
+        self.proc.terminate()
+        try:
+            self.out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            self.out, _ = self.proc.communicate()
+
+    def summary(self):
+        import datetime
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        rows = []
+        for line in (self.out or "").strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                rows.append((ts, float(parts[1]), float(parts[2]), parts[4:8]))
+            except ValueError:
+                continue
+        inside = [r for r in rows if self.t0 is not None and self.t0 <= r[0] <= (self.t1 or 1e18)]
+        use = inside or rows
+        if not use:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        reasons = sorted({n for r in use for n, v in zip(names, r[3]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[1] for r in use), "sm_max_mhz": max(r[2] for r in use),
+                "reasons": reasons, "samples": len(use), "in_window": bool(inside)}
+
+
+# ----------------------------------------------------------------- GPU arm
+class DecodeBench:
+    def __init__(self, device, rank, replicas=REPLICAS, tokens=DECODE_TOKENS):
+        import torch
+        import synth.gpu as sg
+        import quantized_expert_ffn_sigmoid_gb300 as cm
+        self.torch, self.cm = torch, cm
+        self.dev = device
+        self.shape = synth.GLM
+        self.seed = synth.WORKLOADS["glm_decode_b1"][1]
+        self.n = tokens
+        self.R = replicas
+        self.cfg = cm.Cfg.of(self.shape)
+        t0 = time.time()
+        recs, scs = sg.expert_records(self.shape, self.seed, 0, "routed", self.shape.n_experts, device)
+        srec, ssc = sg.expert_records(self.shape, self.seed, 0, "shared", 1, device)
+        wr = torch.from_numpy(synth.router_weight(self.shape, self.seed)).to(device)
+        bias = torch.from_numpy(synth.router_bias(self.shape, self.seed)).to(device)
+        self.rep = []
+        for r in range(self.R):
+            if r == 0:
+                t = (recs, scs, srec, ssc, wr, bias)
+            else:
+                t = tuple(a.clone() for a in (recs, scs, srec, ssc, wr, bias))
+            self.rep.append(t)
+        self.W = [cm.make_weights(t[0], t[1], t[2], t[3]) for t in self.rep]
+        torch.cuda.synchronize()
+        log(f"[bench] weights: {self.R} x {(recs.numel() + srec.numel()) / 1e9:.2f} GB in {time.time() - t0:.1f}s")
+        self.x = sg.token_batch(self.shape, self.seed, ("bench", rank), range(self.n), device)
+        k = self.shape.top_k
+        self.idx = torch.empty((self.n, k), dtype=torch.int32, device=device)
+        self.w = torch.empty((self.n, k), dtype=torch.float32, device=device)
+        self.y = torch.empty((self.n, self.shape.hidden), dtype=torch.float32, device=device)
+        self.ws = cm.new_workspace(self.cfg, 1)
+        self.launches_per_token = 4   # route logits, route select, dispatch, experts
+
+    def step(self):
+        cm = self.cm
+        for i in range(self.n):
+            r = i % self.R
+            rec = self.rep[r]
+            xi = self.x[i:i + 1]
+            cm.coli_moe_route(self.cfg, xi, rec[4], rec[5], self.idx[i:i + 1], self.w[i:i + 1], self.ws)
+            cm.coli_moe_forward(self.cfg, self.W[r], xi, self.idx[i:i + 1], self.w[i:i + 1],
+                                self.y[i:i + 1], self.ws)
+
+    def capture(self):
+        torch = self.torch
+        self.step()  # warm the attribute calls outside capture
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, capture_error_mode="thread_local"):
+            self.step()
+        torch.cuda.synchronize()
+        self.graph = g
+
+    def expert_kernel_ms(self, n=None):
+        """Average expert-kernel duration (CUDA events on its stream); the
+        host enqueues everything behind a sleep so launches are back to back."""
+        torch, cm = self.torch, self.cm
+        n = n or self.n
+        starts = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+        ends = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+        torch.cuda.synchronize()
+        torch.cuda._sleep(int(6e8))   # keeps the GPU busy while the host enqueues
+        for i in range(n):
+            r = i % self.R
+            rec = self.rep[r]
+            xi = self.x[i:i + 1]
+            cm.coli_moe_route(self.cfg, xi, rec[4], rec[5], self.idx[i:i + 1], self.w[i:i + 1], self.ws)
+            cm.coli_moe_dispatch(self.cfg, xi, self.idx[i:i + 1], self.ws)
+            starts[i].record()
+            cm.coli_moe_experts(self.cfg, self.W[r], 1, self.w[i:i + 1], self.y[i:i + 1], self.ws)
+            ends[i].record()
+        torch.cuda.synchronize()
+        d = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+        return statistics.mean(d), statistics.median(d)
+
+    def e2e_step(self, x_host, y_host):
+        """Public API per position with host buffers (copies inside)."""
+        cm = self.cm
+        self.x.copy_(x_host, non_blocking=True)
+        self.step()
+        y_host.copy_(self.y, non_blocking=True)
+        self.torch.cuda.synchronize()
+
+
+def run_gpu(args):
+    import torch
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    b = DecodeBench(device, rank, replicas=args.replicas, tokens=args.tokens)
+    b.capture()
+    for _ in range(args.warmup):
+        b.graph.replay()
+    torch.cuda.synchronize()
+    st = cm_status(b)
+    if st:
+        raise RuntimeError(f"device status {st} after warm-up")
+
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        barrier()
+        clk.mark_start()
+        e0.record()
+        for _ in range(args.steps):
+            b.graph.replay()
+        e1.record()
+        barrier()
+        clk.mark_end()
+    ms = e0.elapsed_time(e1)
+    ms_max = max_over_ranks(ms, world, device)
+    tokens = sum_over_ranks(float(args.steps * b.n), world, device)
+    value = tokens / (ms_max / 1e3)
+
+    # expert kernel alone (roofline of the dominant kernel)
+    k_mean, k_med = b.expert_kernel_ms()
+    hbm, _, peak_kind = read_peaks()
+    kbytes = 9 * EXPERT_BYTES
+    achieved = kbytes / (k_mean / 1e3) / 1e9
+
+    # end to end through the public API with host buffers
+    x_host = b.x.cpu().pin_memory()
+    y_host = torch.empty(b.y.shape, dtype=torch.float32).pin_memory()
+    b.e2e_step(x_host, y_host)
+    barrier()
+    t0 = time.perf_counter()
+    e2e_steps = max(1, min(args.steps, 5))
+    for _ in range(e2e_steps):
+        b.e2e_step(x_host, y_host)
+    barrier()
+    e2e_s = max_over_ranks(time.perf_counter() - t0, world, device)
+    e2e_val = sum_over_ranks(float(e2e_steps * b.n), world, device) / e2e_s
+    st = cm_status(b)
+
+    out = {
+        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_max / args.steps, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int8",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD, "positions_per_call": 1, "positions_per_step": b.n,
+                   "l2": f"inputs larger than L2: {b.R} identical weight copies rotated per call "
+                         f"({b.R * (256 + 1) * EXPERT_BYTES / 1e9:.1f} GB)",
+                   "launch": "CUDA graph of the per-position C-ABI calls",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "layer_bytes_per_token": 9 * EXPERT_BYTES + ROUTER_BYTES,
+                   "layer_gbs": round(value / world * (9 * EXPERT_BYTES + ROUTER_BYTES) / 1e9, 1)},
+        "roofline": {"bound": "hbm", "kernel": "experts_kernel", "achieved": round(achieved, 1),
+                     "peak": hbm, "unit": "GB/s", "frac": round(achieved / hbm, 4),
+                     "peak_source": f"{peak_kind} (HBM copy)", "traffic": args.traffic,
+                     "bytes_per_launch": kbytes, "launch_ms_mean": round(k_mean, 5),
+                     "launch_ms_median": round(k_med, 5)},
+        "e2e": {"value": round(e2e_val, 1), "unit": UNIT, "h2d_bytes_per_step": int(b.x.numel() * 4),
+                "d2h_bytes_per_step": int(b.y.numel() * 4)},
+        "gpu_launches": int(args.steps * b.n * b.launches_per_token),
+        "clocks": clk.summary(),
+        "status": st,
+    }
+    if rank == 0 and args.secondary:
+        out["secondary"] = secondary(device, b)
+    if rank == 0 and not args.no_cpu:
+        out["cpu_baseline"] = cpu_baseline(b, args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def cm_status(b):
+    return b.cm.coli_moe_status(b.ws)
+
+
+def secondary(device, b):
+    """Other workloads on the same resident experts, one graph replay each:
+    MTP verify (4 positions/call) and prefill (2048 positions/call)."""
+    import torch
+    cm = b.cm
+    res = {}
+    shape = b.shape
+    # MTP verify: 4 correlated positions per call
+    seed = synth.WORKLOADS["glm_mtp_verify_t4"][1]
+    calls = 100
+    xs = np.stack([synth.mtp_chain(shape, seed, c) for c in range(calls)])
+    x = torch.from_numpy(xs).to(device)
+    wr = torch.from_numpy(synth.router_weight(shape, seed)).to(device)
+    bias = torch.from_numpy(synth.router_bias(shape, seed)).to(device)
+    ws = cm.new_workspace(b.cfg, 4)
+    idx = torch.empty((calls, 4, 8), dtype=torch.int32, device=device)
+    w = torch.empty((calls, 4, 8), dtype=torch.float32, device=device)
+    y = torch.empty((calls, 4, shape.hidden), dtype=torch.float32, device=device)
+    L = cm.coli_moe_workspace_layout(b.cfg, 4)
+    uniq = 0
+    for c in range(calls):
+        cm.coli_moe_route(b.cfg, x[c], wr, bias, idx[c], w[c], ws)
+        cm.coli_moe_dispatch(b.cfg, x[c], idx[c], ws)
+        uniq += int(ws[L.n_entries:L.n_entries + 4].view(torch.int32).item()) - 1
+
+    wrs = [wr] + [wr.clone() for _ in range(b.R - 1)]
+
+    def mtp():
+        for c in range(calls):
+            r = c % b.R
+            cm.coli_moe_route(b.cfg, x[c], wrs[r], bias, idx[c], w[c], ws)
+            cm.coli_moe_forward(b.cfg, b.W[r], x[c], idx[c], w[c], y[c], ws)
+    ms = time_graph(mtp, 3)
+    byt = (uniq + calls) * EXPERT_BYTES + calls * ROUTER_BYTES
+    res["glm_mtp_verify_t4"] = {"tokens_per_s": round(4 * calls / (ms / 1e3), 1),
+                                "unique_experts_per_call": round(uniq / calls, 2),
+                                "gbs": round(byt / (ms / 1e3) / 1e9, 1), "ms_per_call": round(ms / calls, 4),
+                                "note": "router of the MTP workload, routed experts of the decode workload"}
+    # prefill: 2048 positions, uniform routing
+    seed = synth.WORKLOADS["glm_prefill_s2048"][1]
+    import synth.gpu as sg
+    T = 2048
+    xp = sg.token_batch(shape, seed, 0, range(T), device)
+    wr = torch.from_numpy(synth.router_weight(shape, seed)).to(device)
+    bias = torch.from_numpy(synth.zero_router_bias(shape)).to(device)
+    ws = cm.new_workspace(b.cfg, T)
+    idx = torch.empty((T, 8), dtype=torch.int32, device=device)
+    w = torch.empty((T, 8), dtype=torch.float32, device=device)
+    y = torch.empty((T, shape.hidden), dtype=torch.float32, device=device)
+
+    def pre():
+        cm.coli_moe_route(b.cfg, xp, wr, bias, idx, w, ws)
+        cm.coli_moe_forward(b.cfg, b.W[0], xp, idx, w, y, ws)
+    ms = time_graph(pre, 2)
+    ops = 2.0 * (T * 8 + T) * 3 * shape.inter * shape.hidden
+    byt = (256 + 1) * EXPERT_BYTES + ROUTER_BYTES
+    res["glm_prefill_s2048"] = {"tokens_per_s": round(T / (ms / 1e3), 1), "ms_per_call": round(ms, 3),
+                                "int8_tops": round(ops / (ms / 1e3) / 1e12, 2),
+                                "gbs_min_bytes": round(byt / (ms / 1e3) / 1e9, 1)}
+    return res
+
+
+def time_graph(fn, reps):
+    import torch
+    fn()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, capture_error_mode="thread_local"):
+        fn()
+    g.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        g.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / reps
+
+
+# ----------------------------------------------------------------- CPU oracle
+def oracle_tokens_per_s(get_record, router_w, bias, xs, budget_s):
+    """The oracle as it stands, one position per call, until ``budget_s``."""
+    import oracle
+    shape = synth.GLM
+    n = 0
+    t0 = time.perf_counter()
+    while n < len(xs):
+        oracle.moe_layer(shape, get_record, xs[n:n + 1], router_w, bias)
+        n += 1
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    return n, time.perf_counter() - t0
+
+
+def host_records(recs, scs, srec, ssc):
+    """Host copies of a layer's records (generator output), made before any timing."""
+    R, S, SR, SS = recs.cpu().numpy(), scs.cpu().numpy(), srec.cpu().numpy(), ssc.cpu().numpy()
+    return lambda kind, e: (R[e], S[e]) if kind == "routed" else (SR[e], SS[e])
+
+
+def cpu_baseline(b, budget_s):
+    xs = b.x[:16].cpu().numpy()
+    rep = b.rep[0]
+    get_record = host_records(rep[0], rep[1], rep[2], rep[3])
+    wr = rep[4].cpu().numpy()
+    bias = rep[5].cpu().numpy()
+    n, s = oracle_tokens_per_s(get_record, wr, bias, xs, budget_s)
+    return {"value": round(n / s, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"{n} positions of the decode workload, one layer call each (numpy, 1 thread)"}
+
+
+def run_reference(args):
+    """The oracle as the reference arm: same workload, metric and unit."""
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle  # noqa: F401
+    shape = synth.GLM
+    seed = synth.WORKLOADS["glm_decode_b1"][1]
+    wr = synth.router_weight(shape, seed)
+    bias = synth.router_bias(shape, seed)
+    xs = synth.token_batch(shape, seed, ("bench", 0), range(args.warmup + args.steps))
+    # the layer's records, made by the generator before any timing (on the
+    # device twin when a GPU is present: 4.9 GB in seconds instead of minutes)
+    try:
+        import torch
+        import synth.gpu as sg
+        if not torch.cuda.is_available():
+            raise RuntimeError
+        recs, scs = sg.expert_records(shape, seed, 0, "routed", shape.n_experts, "cuda")
+        srec, ssc = sg.expert_records(shape, seed, 0, "shared", 1, "cuda")
+        get_record = host_records(recs, scs, srec, ssc)
+        del recs, scs, srec, ssc
+    except (ImportError, RuntimeError, OSError):
+        import oracle as _o
+        need = set()
+        idx, _ = _o.route(_o.router_logits(xs, wr), bias, shape)
+        need.update(int(e) for e in idx.ravel())
+        cache = {("routed", e): synth.expert_record(shape, seed, 0, "routed", e) for e in sorted(need)}
+        cache[("shared", 0)] = synth.expert_record(shape, seed, 0, "shared", 0)
+        get_record = lambda kind, e: cache[(kind, e)]
+    per_step = 1
+    for i in range(args.warmup):
+        oracle_tokens_per_s(get_record, wr, bias, xs[i:i + 1], 1e9)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        oracle_tokens_per_s(get_record, wr, bias, xs[args.warmup + i:args.warmup + i + 1], 1e9)
+    s = time.perf_counter() - t0
+    value = args.steps * per_step / s
+    out = {"metric": METRIC, "value": round(value, 4), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+           "warmup": args.warmup, "ms_per_step": round(1e3 * s / args.steps, 2), "higher_is_better": True,
+           "scaling": "weak", "vs_baseline": None, "dtype": "int8", "data": "synthetic", "impl": "reference",
+           "config": {"workload": WORKLOAD, "positions_per_step": per_step},
+           "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
+                            "sample": f"{per_step} position per step of the decode workload (numpy, 1 thread)"},
+           "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(out), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=40)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--replicas", type=int, default=REPLICAS)
+    ap.add_argument("--tokens", type=int, default=DECODE_TOKENS)
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    ap.add_argument("--no-secondary", dest="secondary", action="store_false")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--traffic", type=float, default=None,
+                    help="ncu dram bytes per expert-kernel launch, if measured for this build")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "gb300" and args.steps > 2:
+        log("[bench] warm-up raised to 3")
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()
