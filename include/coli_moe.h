@@ -199,6 +199,34 @@ int coli_moe_forward_dump(const coli_moe_cfg* cfg, const coli_moe_weights* weigh
                           void* ws, size_t ws_bytes,
                           int32_t* acc_gu, int32_t* acc_d, cudaStream_t stream);
 
+/* ---- no-allocation variant ----------------------------------------------
+ * The pages have no counterpart to this entry point; it exists for callers
+ * that cannot allocate device memory to pass a workspace -- a plain C or FFI
+ * host that links only this library and owns no allocator, or a runtime that
+ * keeps the whole device-memory budget and forbids stray cudaMalloc calls.
+ *
+ * coli_moe_forward_static computes exactly what coli_moe_forward computes,
+ * with its workspace taken from one static device array of
+ * COLI_STATIC_WS_BYTES inside the library (held on every GPU that loads the
+ * library until the process exits).  It calls no cudaMalloc, cudaFree or
+ * other allocating routine.  The caller still passes x, routing and y.
+ *   - Limit: the layer's workspace for T positions must fit in
+ *     COLI_STATIC_WS_BYTES (16 MiB: the GLM-5.2-shaped layer up to T = 66);
+ *     larger T returns COLI_EWORKSPACE and enqueues nothing.
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress, with that device current) and caches it; make
+ *     that first call before any stream capture.
+ *   - Every call on a device shares the one array: calls that overlap on the
+ *     GPU (different streams, or host threads without ordering) race and give
+ *     wrong results.  Calls ordered on one stream are safe; each call rewrites
+ *     every table and counter it reads.
+ *   - Device status bits (non-finite input, bad ids) are not reported. */
+#define COLI_STATIC_WS_BYTES (16u << 20)
+int coli_moe_forward_static(const coli_moe_cfg* cfg, const coli_moe_weights* weights,
+                            const float* x, int32_t T,
+                            const int32_t* topk_idx, const float* topk_w, float* y,
+                            cudaStream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

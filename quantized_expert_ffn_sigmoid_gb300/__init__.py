@@ -29,8 +29,9 @@ EXPORTS = (
     "coli_moe_workspace_size", "coli_moe_workspace_init", "coli_moe_route",
     "coli_moe_quantize_act", "coli_moe_forward", "coli_moe_dispatch", "coli_moe_experts",
     "coli_moe_status", "coli_moe_strerror", "coli_moe_workspace_layout",
-    "coli_moe_forward_dump",
+    "coli_moe_forward_dump", "coli_moe_forward_static",
 )
+STATIC_WS_BYTES = 16 << 20
 
 
 class Cfg(ctypes.Structure):
@@ -76,6 +77,7 @@ def _load():
         "coli_moe_strerror": ([ctypes.c_int], ctypes.c_char_p),
         "coli_moe_workspace_layout": ([CP, I32, ctypes.POINTER(WsLayout)], ctypes.c_int),
         "coli_moe_forward_dump": ([CP, WP, P, I32, P, P, P, P, S, P, P, P], ctypes.c_int),
+        "coli_moe_forward_static": ([CP, WP, P, I32, P, P, P, P], ctypes.c_int),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -193,3 +195,12 @@ def coli_moe_workspace_layout(cfg, T: int) -> WsLayout:
     _check(lib.coli_moe_workspace_layout(ctypes.byref(_cfg(cfg)), int(T), ctypes.byref(out)),
            "coli_moe_workspace_layout")
     return out
+
+
+def coli_moe_forward_static(cfg, weights: Weights, x, topk_idx, topk_w, y, stream=None):
+    """coli_moe_forward without a caller workspace: the library's static
+    16 MiB device scratch is used instead (for callers that cannot allocate;
+    calls must not overlap on the GPU)."""
+    _check(lib.coli_moe_forward_static(ctypes.byref(_cfg(cfg)), ctypes.byref(weights), _ptr(x), x.shape[0],
+                                       _ptr(topk_idx), _ptr(topk_w), _ptr(y), _stream(stream)),
+           "coli_moe_forward_static")
