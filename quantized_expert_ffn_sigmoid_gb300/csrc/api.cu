@@ -12,6 +12,7 @@ cudaError_t launch_quantize_act(const float* x, long long nblk, int8_t* q, float
                                 cudaStream_t st);
 cudaError_t launch_prep(const PrepParams& P, unsigned grid, size_t smem, cudaStream_t st);
 cudaError_t launch_experts(const ExpertParams& P, int grid, size_t smem, cudaStream_t st, bool dump);
+cudaError_t launch_gemv(const ExpertParams& P, int n_sm, cudaStream_t st, bool dump);
 size_t experts_smem_bytes(const coli_moe_cfg& c, const Layout& L);
 }  // namespace colimoe
 
@@ -93,6 +94,12 @@ int do_experts(const coli_moe_cfg& c, const coli_moe_weights* w, int T, const fl
   P.L = L;
   P.dump_gu = dump_gu;
   P.dump_d = dump_d;
+  if (T <= GEMV_MAX_T) {
+    // a few positions: stream the weights through the two GEMV kernels
+    const int n_sm = sm_count();
+    if (n_sm <= 0) return COLI_ECUDA;
+    return rc_of(launch_gemv(P, n_sm, st, dump_gu || dump_d));
+  }
   const size_t smem = experts_smem_bytes(c, L);
   int dev_smem = 0, dev = 0;
   cudaGetDevice(&dev);

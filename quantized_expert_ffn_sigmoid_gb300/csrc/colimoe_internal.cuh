@@ -26,6 +26,9 @@ constexpr int MAX_GROUPS = 32;
 constexpr int GEMV_SPLITS = 8;  // K splits of the router GEMV (T <= 8)
 constexpr int ROUTE_GEMV_MAX_T = 8;
 constexpr int PREP_THREADS = 1024;
+constexpr int GEMV_MAX_T = 8;   // calls up to this many positions take the streaming GEMV path
+constexpr int GU_THREADS = 256; // gate/up GEMV: 8 warps, 4 row pairs each (one 32-row tile)
+constexpr int DN_ROWS = 16;     // down GEMV: output rows per CTA (4 warps x 4 rows)
 constexpr uint32_t SPIN_LIMIT = 1u << 22;  // bounded waits (about a second or more)
 
 __host__ __device__ inline int row_bytes(int k, int bits) { return bits == 4 ? k / 2 : k; }
@@ -52,7 +55,7 @@ __host__ __device__ inline size_t align_up(size_t v, size_t a) { return (v + a -
 struct Layout {
   int T, P, n_ent_max, n_tiles, imax;
   size_t status, counters, hdr, ent_expert, ent_count, ent_offset, ent_item_a,
-         ent_item_b, pair_token, slot, route_part, qx, dx, xs, qh, dh, hs, o, total;
+         ent_item_b, pair_token, pair_j, slot, route_part, qx, dx, xs, qh, dh, hs, o, total;
 };
 // Table header (ints at Layout::hdr)
 enum HdrField { H_NENT = 0, H_NUNIQ, H_NA, H_NB, H_BTARGET, H_NPAIRS, H_FIELDS = 8 };
@@ -79,6 +82,7 @@ __host__ __device__ inline Layout make_layout(const coli_moe_cfg& c, int T) {
   L.ent_item_a = take(4 * ((size_t)L.n_ent_max + 1));
   L.ent_item_b = take(4 * ((size_t)L.n_ent_max + 1));
   L.pair_token = take(4 * (size_t)L.P);
+  L.pair_j = take(4 * (size_t)L.P);
   L.slot = take(4 * (size_t)T * k);
   size_t gemv = (size_t)GEMV_SPLITS * (T < ROUTE_GEMV_MAX_T ? T : ROUTE_GEMV_MAX_T) * E;
   size_t tiled = (size_t)T * E;

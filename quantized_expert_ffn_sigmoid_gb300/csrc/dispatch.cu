@@ -113,6 +113,7 @@ __global__ void __launch_bounds__(PREP_THREADS) prep_kernel(PrepParams P) {
   int32_t* ent_item_a = reinterpret_cast<int32_t*>(ws + L.ent_item_a);
   int32_t* ent_item_b = reinterpret_cast<int32_t*>(ws + L.ent_item_b);
   int32_t* pair_token = reinterpret_cast<int32_t*>(ws + L.pair_token);
+  int32_t* pair_j = reinterpret_cast<int32_t*>(ws + L.pair_j);
   int32_t* slot = reinterpret_cast<int32_t*>(ws + L.slot);
 
   for (int i = tid; i < 1 + L.n_ent_max + L.n_tiles; i += PREP_THREADS) ctr[i] = 0u;
@@ -150,7 +151,10 @@ __global__ void __launch_bounds__(PREP_THREADS) prep_kernel(PrepParams P) {
     ent_offset[n_uniq + s] = total_pairs + s * T;
   }
   if (tid == 0) ent_offset[n_ent] = total_pairs + ns * T;
-  for (int i = tid; i < ns * T; i += PREP_THREADS) pair_token[total_pairs + i] = i % T;
+  for (int i = tid; i < ns * T; i += PREP_THREADS) {
+    pair_token[total_pairs + i] = i % T;
+    pair_j[total_pairs + i] = -1;
+  }
   __syncthreads();
 
   // ranks inside each routed entry in (t, j) order, chunk by chunk
@@ -170,6 +174,7 @@ __global__ void __launch_bounds__(PREP_THREADS) prep_kernel(PrepParams P) {
         for (int w = 0; w < warp; ++w) pre += wcnt[w * E + e];
         const int sl = eoff[e] + run[e] + pre + lrank;
         pair_token[sl] = p / k;
+        pair_j[sl] = p % k;
         slot[p] = sl;
       } else {
         slot[p] = -1;

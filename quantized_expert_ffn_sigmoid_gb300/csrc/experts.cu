@@ -104,17 +104,18 @@ struct BlockW {
     }
   }
   __device__ __forceinline__ int dot(const uint4& a0, const uint4& a1, int corr) const {
-    int s = 0;
+    // two independent dp4a chains (latency), joined at the end
+    int s = 0, r = 0;
     if (BITS == 4) {
-      s = dp4a_us(v[0], a0.x, s); s = dp4a_us(v[1], a0.y, s); s = dp4a_us(v[2], a0.z, s);
-      s = dp4a_us(v[3], a0.w, s); s = dp4a_us(v[4], a1.x, s); s = dp4a_us(v[5], a1.y, s);
-      s = dp4a_us(v[6], a1.z, s); s = dp4a_us(v[7], a1.w, s);
-      return s - corr;
+      s = dp4a_us(v[0], a0.x, s); r = dp4a_us(v[1], a0.y, r); s = dp4a_us(v[2], a0.z, s);
+      r = dp4a_us(v[3], a0.w, r); s = dp4a_us(v[4], a1.x, s); r = dp4a_us(v[5], a1.y, r);
+      s = dp4a_us(v[6], a1.z, s); r = dp4a_us(v[7], a1.w, r);
+      return (s + r) - corr;
     } else {
-      s = dp4a_ss(v[0], a0.x, s); s = dp4a_ss(v[1], a0.y, s); s = dp4a_ss(v[2], a0.z, s);
-      s = dp4a_ss(v[3], a0.w, s); s = dp4a_ss(v[4], a1.x, s); s = dp4a_ss(v[5], a1.y, s);
-      s = dp4a_ss(v[6], a1.z, s); s = dp4a_ss(v[7], a1.w, s);
-      return s;
+      s = dp4a_ss(v[0], a0.x, s); r = dp4a_ss(v[1], a0.y, r); s = dp4a_ss(v[2], a0.z, s);
+      r = dp4a_ss(v[3], a0.w, r); s = dp4a_ss(v[4], a1.x, s); r = dp4a_ss(v[5], a1.y, r);
+      s = dp4a_ss(v[6], a1.z, s); r = dp4a_ss(v[7], a1.w, r);
+      return s + r;
     }
   }
 };
@@ -137,6 +138,54 @@ __device__ __forceinline__ const uint8_t* entry_record(const ExpertParams& P, in
 }
 
 // ---------------------------------------------------------------- producer
+// A decoded work item plus the positions it needs (loaded one item ahead so
+// that their latency hides behind the previous item's weight stream).
+struct Pending {
+  ItemDesc d;
+  const uint8_t* rec;
+  int tok[TG];
+};
+
+template <int BITS>
+__device__ __forceinline__ Pending decode_ticket(const ExpertParams& P, const SmemPtrs& S, uint32_t ticket,
+                                                 int nA, int nB, int n_ent) {
+  Pending pd;
+  ItemDesc& d = pd.d;
+  d = ItemDesc{};
+  pd.rec = nullptr;
+  if (ticket >= (uint32_t)(nA + nB)) {
+    d.kind = 2;
+    return pd;
+  }
+  const bool isA = ticket < (uint32_t)nA;
+  const int local = isA ? (int)ticket : (int)ticket - nA;
+  const int* pref = isA ? S.t_item_a : S.t_item_b;
+  int lo = 0, hi = n_ent - 1;  // largest u with pref[u] <= local
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (pref[mid] <= local) lo = mid; else hi = mid - 1;
+  }
+  const int u = lo;
+  const int cnt = S.t_count[u];
+  const int ntg = (cnt + TG - 1) / TG;
+  const int li = local - pref[u];
+  d.kind = isA ? 0 : 1;
+  d.ent = u;
+  d.tile = li / ntg;
+  const int tg = li % ntg;
+  d.ntok = min(TG, cnt - tg * TG);
+  d.pair0 = S.t_offset[u] + tg * TG;
+  d.expert = S.t_expert[u];
+  const float* scales;
+  pd.rec = entry_record(P, d.expert, &d.inter, &scales);
+  if (isA) {
+    const int32_t* pair_token = reinterpret_cast<const int32_t*>(P.ws + P.L.pair_token);
+#pragma unroll
+    for (int i = 0; i < TG; ++i) pd.tok[i] = i < d.ntok ? __ldcg(pair_token + d.pair0 + i) : 0;
+  }
+  return pd;
+}
+
 template <int BITS>
 __device__ void producer_loop(const ExpertParams& P, const SmemPtrs& S, int nA, int nB, int n_ent) {
   const coli_moe_cfg& c = P.cfg;
@@ -144,7 +193,6 @@ __device__ void producer_loop(const ExpertParams& P, const SmemPtrs& S, int nA, 
   uint8_t* ws = P.ws;
   uint32_t* status = reinterpret_cast<uint32_t*>(ws + L.status);
   uint32_t* ctr = reinterpret_cast<uint32_t*>(ws + L.counters);
-  const int32_t* pair_token = reinterpret_cast<const int32_t*>(ws + L.pair_token);
   const int H = c.hidden;
   const int nbH = H / QB;
   const int rbA = row_bytes(H, BITS);
@@ -153,99 +201,81 @@ __device__ void producer_loop(const ExpertParams& P, const SmemPtrs& S, int nA, 
   const uint64_t pol_w = policy_evict_first();
   const uint64_t pol_a = policy_evict_last();
   uint32_t stage = 0, item = 0;
-  for (;;) {
-    const uint32_t ticket = atomicAdd(&ctr[0], 1u);
+  Pending cur = decode_ticket<BITS>(P, S, atomicAdd(&ctr[0], 1u), nA, nB, n_ent);
+  uint32_t next_ticket = atomicAdd(&ctr[0], 1u);
+  for (;; ++item) {
     const int as = item & 1;
+    const ItemDesc& d = cur.d;
     mbar_wait(&S.aempty[as], ((item >> 1) & 1u) ^ 1u, status);
-    ItemDesc d{};
-    if (ticket >= (uint32_t)(nA + nB)) {
-      d.kind = 2;
-      S.desc[as] = d;
+    S.desc[as] = d;
+    if (d.kind == 2) {
       mbar_arrive(&S.afull[as]);
       break;
     }
-    const bool isA = ticket < (uint32_t)nA;
-    const int local = isA ? (int)ticket : (int)ticket - nA;
-    const int* pref = isA ? S.t_item_a : S.t_item_b;
-    int lo = 0, hi = n_ent - 1;  // largest u with pref[u] <= local
-    while (lo < hi) {
-      int mid = (lo + hi + 1) >> 1;
-      if (pref[mid] <= local) lo = mid; else hi = mid - 1;
-    }
-    const int u = lo;
-    const int cnt = S.t_count[u];
-    const int ntg = (cnt + TG - 1) / TG;
-    const int li = local - pref[u];
-    const int tile = li / ntg, tg = li % ntg;
-    d.kind = isA ? 0 : 1;
-    d.ent = u;
-    d.tile = tile;
-    d.ntok = min(TG, cnt - tg * TG);
-    d.pair0 = S.t_offset[u] + tg * TG;
-    d.expert = S.t_expert[u];
-    const float* scales;
-    const uint8_t* rec = entry_record(P, d.expert, &d.inter, &scales);
-    S.desc[as] = d;
-
     uint8_t* A = S.act + as * slot_bytes;
-    if (isA) {
-      const int32_t tokbytes = H + 2 * nbH * 4;
-      mbar_arrive_expect_tx(&S.afull[as], (uint32_t)(d.ntok * tokbytes));
-      for (int i = 0; i < d.ntok; ++i) {
-        const int t = pair_token[d.pair0 + i];
-        bulk_g2s(A + i * H, ws + L.qx + (size_t)t * H, H, &S.afull[as], pol_a);
-        bulk_g2s(A + TG * H + i * nbH * 4, ws + L.dx + (size_t)t * nbH * 4, nbH * 4, &S.afull[as], pol_a);
-        bulk_g2s(A + TG * H + TG * nbH * 4 + i * nbH * 4, ws + L.xs + (size_t)t * nbH * 4, nbH * 4,
-                 &S.afull[as], pol_a);
+    if (d.kind == 0) {
+      const uint32_t tokbytes = (uint32_t)(H + 2 * nbH * 4);
+      mbar_arrive_expect_tx(&S.afull[as], (uint32_t)d.ntok * tokbytes);
+#pragma unroll
+      for (int i = 0; i < TG; ++i) {
+        if (i < d.ntok) {
+          const int t = cur.tok[i];
+          bulk_g2s(A + i * H, ws + L.qx + (size_t)t * H, H, &S.afull[as], pol_a);
+          bulk_g2s(A + TG * H + i * nbH * 4, ws + L.dx + (size_t)t * nbH * 4, nbH * 4, &S.afull[as], pol_a);
+          bulk_g2s(A + TG * H + TG * nbH * 4 + i * nbH * 4, ws + L.xs + (size_t)t * nbH * 4, nbH * 4,
+                   &S.afull[as], pol_a);
+        }
       }
     } else {
       // down products need every h block of this entry
-      const uint32_t target = (uint32_t)(S.t_item_a[u + 1] - S.t_item_a[u]);
-      uint32_t* done = &ctr[1 + u];
+      const uint32_t target = (uint32_t)(S.t_item_a[d.ent + 1] - S.t_item_a[d.ent]);
+      const uint32_t* done = &ctr[1 + d.ent];
       bool ok = false;
       for (uint32_t i = 0; i < SPIN_LIMIT; ++i) {
         if (ld_acquire_u32(done) >= target) { ok = true; break; }
-        __nanosleep(128);
+        __nanosleep(64);
       }
       if (!ok) atomicOr(status, COLI_STATUS_TIMEOUT);
       fence_proxy_async_global();
       const int im = L.imax, nbI = im / QB;
-      const uint32_t bytes = (uint32_t)d.ntok * (im + 2 * nbI * 4);
-      mbar_arrive_expect_tx(&S.afull[as], bytes);
+      mbar_arrive_expect_tx(&S.afull[as], (uint32_t)d.ntok * (im + 2 * nbI * 4));
       bulk_g2s(A, ws + L.qh + (size_t)d.pair0 * im, d.ntok * im, &S.afull[as], pol_a);
       bulk_g2s(A + TG * im, ws + L.dh + (size_t)d.pair0 * nbI * 4, d.ntok * nbI * 4, &S.afull[as], pol_a);
       bulk_g2s(A + TG * im + TG * nbI * 4, ws + L.hs + (size_t)d.pair0 * nbI * 4, d.ntok * nbI * 4,
                &S.afull[as], pol_a);
     }
+    // look one item ahead: its ticket and positions load while this item's
+    // weight stages stream
+    const Pending nxt = decode_ticket<BITS>(P, S, next_ticket, nA, nB, n_ent);
+    if (nxt.d.kind != 2) next_ticket = atomicAdd(&ctr[0], 1u);
 
-    // weight stages
-    if (isA) {
+    if (d.kind == 0) {
       const int nst = RA / rsA;
       const uint32_t bytes = (uint32_t)rsA * rbA;
       for (int st = 0; st < nst; ++st, ++stage) {
         const int s = stage % NS;
         mbar_wait(&S.empty[s], ((stage / NS) & 1u) ^ 1u, status);
-        const int row0 = tile * RA + st * rsA;
+        const int row0 = d.tile * RA + st * rsA;
         uint8_t* dst = S.ring + (size_t)s * SB;
         mbar_arrive_expect_tx(&S.full[s], 2 * bytes);
-        bulk_g2s(dst, rec + (size_t)row0 * rbA, bytes, &S.full[s], pol_w);
-        bulk_g2s(dst + bytes, rec + (size_t)d.inter * rbA + (size_t)row0 * rbA, bytes, &S.full[s], pol_w);
+        bulk_g2s(dst, cur.rec + (size_t)row0 * rbA, bytes, &S.full[s], pol_w);
+        bulk_g2s(dst + bytes, cur.rec + (size_t)d.inter * rbA + (size_t)row0 * rbA, bytes, &S.full[s], pol_w);
       }
     } else {
       const int rbB = row_bytes(d.inter, BITS);
       const int rsB = stage_rows_b(d.inter, BITS);
       const int nst = RB / rsB;
       const uint32_t bytes = (uint32_t)rsB * rbB;
-      const uint8_t* down = rec + (size_t)2 * d.inter * rbA;
+      const uint8_t* down = cur.rec + (size_t)2 * d.inter * rbA;
       for (int st = 0; st < nst; ++st, ++stage) {
         const int s = stage % NS;
         mbar_wait(&S.empty[s], ((stage / NS) & 1u) ^ 1u, status);
-        const int row0 = tile * RB + st * rsB;
+        const int row0 = d.tile * RB + st * rsB;
         mbar_arrive_expect_tx(&S.full[s], bytes);
         bulk_g2s(S.ring + (size_t)s * SB, down + (size_t)row0 * rbB, bytes, &S.full[s], pol_w);
       }
     }
-    ++item;
+    cur = nxt;
   }
 }
 
@@ -359,7 +389,8 @@ __device__ void finish_a(const ExpertParams& P, const SmemPtrs& S, const ItemDes
       if (bad) atomicOr(status, COLI_STATUS_NONFINITE);
     }
   }
-  __threadfence();
+  // the CTA's qh/dh stores happen-before thread 0's release through the
+  // barrier, and release is cumulative: one gpu-scope release publishes them
   consumer_bar();
   if (cw == 0 && lane == 0) {
     uint32_t* ctr = reinterpret_cast<uint32_t*>(ws + L.counters);
@@ -458,14 +489,14 @@ __device__ void finish_b(const ExpertParams& P, const SmemPtrs& S, const ItemDes
     const int row = d.tile * RB + r;
     o[(size_t)(d.pair0 + t) * H + row] = __fmul_rn(sc[2 * inter + row], sum);
   }
-  __threadfence();
+  // one acq_rel atomic publishes this CTA's o rows (cumulative release after
+  // the barrier) and, for the last arriver, acquires everyone else's
   consumer_bar();
   if (ctid == 0) {
     uint32_t* ctr = reinterpret_cast<uint32_t*>(ws + L.counters);
     const int32_t* hdr = reinterpret_cast<const int32_t*>(ws + L.hdr);
     const uint32_t old = atom_acq_rel_add(&ctr[1 + L.n_ent_max + d.tile], 1u);
     *S.flag = (old + 1u == (uint32_t)hdr[H_BTARGET]) ? 1 : 0;
-    __threadfence();
   }
   consumer_bar();
   if (*S.flag) {
