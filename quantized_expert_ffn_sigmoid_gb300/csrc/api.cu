@@ -7,10 +7,11 @@
 namespace colimoe {
 cudaError_t launch_route(const float* x, int T, int H, const float* wr, int E, int G, int topk_group, int k,
                          float rsf, const float* bias, int32_t* topk_idx, float* topk_w, float* part,
-                         uint32_t* status, cudaStream_t st);
+                         uint32_t* status, uint32_t* counter, cudaStream_t st);
 cudaError_t launch_quantize_act(const float* x, long long nblk, int8_t* q, float* d, unsigned blocks,
                                 cudaStream_t st);
 cudaError_t launch_prep(const PrepParams& P, unsigned grid, size_t smem, cudaStream_t st);
+cudaError_t launch_prep_small(const PrepParams& P, unsigned grid, cudaStream_t st);
 cudaError_t launch_experts(const ExpertParams& P, int grid, size_t smem, cudaStream_t st, bool dump);
 cudaError_t launch_gemv(const ExpertParams& P, int n_sm, cudaStream_t st, bool dump);
 size_t experts_smem_bytes(const coli_moe_cfg& c, const Layout& L);
@@ -73,6 +74,11 @@ size_t prep_smem(const coli_moe_cfg& c) {
 int do_dispatch(const coli_moe_cfg& c, const float* x, int T, const int32_t* idx, uint8_t* ws,
                 const Layout& L, cudaStream_t st) {
   PrepParams P{c, x, idx, T, ws, L};
+  if (T <= GEMV_MAX_T && T * c.top_k <= GEMV_MAX_T * MAX_TOPK) {
+    const int nblk = T * (c.hidden / QB);
+    const unsigned grid = (unsigned)((nblk + 8 * 4 - 1) / (8 * 4));  // ~4 blocks per warp
+    return rc_of(launch_prep_small(P, grid > 0 ? grid : 1, st));
+  }
   const long long nblk = (long long)T * (c.hidden / QB);
   long long nq = (nblk + PREP_THREADS / 32 - 1) / (PREP_THREADS / 32);
   const long long cap = 8LL * (sm_count() > 0 ? sm_count() : 132);
@@ -151,7 +157,8 @@ int coli_moe_route(const coli_moe_cfg* cfg, const float* x, int32_t T, const flo
   return rc_of(launch_route(x, T, c.hidden, router_w, c.n_experts, c.n_groups, c.topk_group, c.top_k,
                             c.routed_scaling_factor, corr_bias, topk_idx, topk_w,
                             reinterpret_cast<float*>(w8 + L.route_part),
-                            reinterpret_cast<uint32_t*>(w8 + L.status), stream));
+                            reinterpret_cast<uint32_t*>(w8 + L.status),
+                            reinterpret_cast<uint32_t*>(w8 + L.status) + 1, stream));
 }
 
 int coli_moe_quantize_act(const float* x, int32_t T, int32_t K, int8_t* q, float* d, cudaStream_t stream) {

@@ -225,6 +225,165 @@ __global__ void __launch_bounds__(PREP_THREADS) prep_kernel(PrepParams P) {
   }
 }
 
+__device__ __forceinline__ void pdl_wait_d() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger_d() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// Dispatch for calls of at most GEMV_MAX_T positions (<= 256 pairs): every
+// warp quantises x blocks first (x is an input, so this overlaps the router
+// still finishing), then warp 0 of block 0 waits for the routing and builds
+// the same canonical tables as prep_kernel with warp-level counting (ranks by
+// comparing the <= 256 keys (expert, pair) in shared memory).
+template <int BITS>
+__global__ void __launch_bounds__(256) prep_small_kernel(PrepParams P) {
+  const coli_moe_cfg& c = P.cfg;
+  const Layout& L = P.L;
+  uint8_t* ws = P.ws;
+  uint32_t* status = reinterpret_cast<uint32_t*>(ws + L.status);
+  const int H = c.hidden, E = c.n_experts, k = c.top_k, T = P.T, ns = c.n_shared;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  {
+    const int nb = H / QB;
+    const int nblk = T * nb;
+    const int warps = gridDim.x * 8;
+    int8_t* qx = reinterpret_cast<int8_t*>(ws + L.qx);
+    float* dx = reinterpret_cast<float*>(ws + L.dx);
+    int32_t* xs = reinterpret_cast<int32_t*>(ws + L.xs);
+    bool anybad = false;
+    for (int b = blockIdx.x * 8 + warp; b < nblk; b += warps) {
+      const float v = P.x[(size_t)b * QB + lane];
+      float dd;
+      bool bad;
+      const int q = q8_0_lane(v, &dd, &bad);
+      anybad |= bad;
+      qx[(size_t)b * QB + (BITS == 4 ? perm8(lane) : lane)] = (int8_t)q;
+      const int sum = warp_sum_i(q);
+      if (lane == 0) {
+        dx[b] = dd;
+        xs[b] = BITS == 4 ? 8 * sum : 0;
+      }
+    }
+    if (anybad && lane == 0) atomicOr(status, COLI_STATUS_NONFINITE);
+  }
+  if (blockIdx.x != 0 || warp != 0) return;
+
+  __shared__ int key[GEMV_MAX_T * MAX_TOPK];
+  __shared__ unsigned char first[GEMV_MAX_T * MAX_TOPK];
+  pdl_wait_d();  // routing comes from the router kernel
+  pdl_trigger_d();
+  uint32_t* ctr = reinterpret_cast<uint32_t*>(ws + L.counters);
+  int32_t* hdr = reinterpret_cast<int32_t*>(ws + L.hdr);
+  int32_t* ent_expert = reinterpret_cast<int32_t*>(ws + L.ent_expert);
+  int32_t* ent_count = reinterpret_cast<int32_t*>(ws + L.ent_count);
+  int32_t* ent_offset = reinterpret_cast<int32_t*>(ws + L.ent_offset);
+  int32_t* ent_item_a = reinterpret_cast<int32_t*>(ws + L.ent_item_a);
+  int32_t* ent_item_b = reinterpret_cast<int32_t*>(ws + L.ent_item_b);
+  int32_t* pair_token = reinterpret_cast<int32_t*>(ws + L.pair_token);
+  int32_t* pair_j = reinterpret_cast<int32_t*>(ws + L.pair_j);
+  int32_t* slot = reinterpret_cast<int32_t*>(ws + L.slot);
+  for (int i = lane; i < 1 + L.n_ent_max + L.n_tiles; i += 32) ctr[i] = 0u;
+
+  const int npair = T * k;  // <= 256
+  bool badidx = false;
+  for (int p = lane; p < npair; p += 32) {
+    const int e = P.idx[p];
+    const bool valid = e >= 0 && e < E;
+    if (!valid && e != -1) badidx = true;
+    key[p] = valid ? (e << 8) | p : 0x7fffffff;
+  }
+  if (__any_sync(0xffffffffu, badidx) && lane == 0) atomicOr(status, COLI_STATUS_BADIDX);
+  __syncwarp();
+  // rank = sorted position of (expert, pair); first = no earlier pair of that expert
+  int nvalid = 0, nfirst = 0;
+  for (int p = lane; p < npair; p += 32) {
+    const int kp = key[p];
+    int rank = 0, before = 0;
+    for (int q = 0; q < npair; ++q) {
+      const int kq = key[q];
+      rank += kq < kp;
+      before += (kq >> 8) == (kp >> 8) && kq < kp;
+    }
+    if (kp != 0x7fffffff) {
+      slot[p] = rank;
+      pair_token[rank] = p / k;
+      pair_j[rank] = p % k;
+    } else {
+      slot[p] = -1;
+    }
+    first[p] = kp != 0x7fffffff && before == 0;
+  }
+  for (int p = lane; p < npair; p += 32) {
+    nvalid += key[p] != 0x7fffffff;
+  }
+  __syncwarp();
+  for (int p = lane; p < npair; p += 32) nfirst += first[p];
+  nvalid = warp_sum_i(nvalid);
+  const int n_uniq = warp_sum_i(nfirst);
+  for (int p = lane; p < npair; p += 32) {
+    if (!first[p]) continue;
+    const int kp = key[p], e = kp >> 8;
+    int ent = 0, cnt = 0, off = 0;
+    for (int q = 0; q < npair; ++q) {
+      const int kq = key[q];
+      ent += first[q] && (kq >> 8) < e;
+      cnt += (kq >> 8) == e;
+      off += kq < kp;
+    }
+    ent_expert[ent] = e;
+    ent_count[ent] = cnt;
+    ent_offset[ent] = off;
+  }
+  for (int s = lane; s < ns; s += 32) {
+    ent_expert[n_uniq + s] = E + s;
+    ent_count[n_uniq + s] = T;
+    ent_offset[n_uniq + s] = nvalid + s * T;
+  }
+  for (int i = lane; i < ns * T; i += 32) {
+    pair_token[nvalid + i] = i % T;
+    pair_j[nvalid + i] = -1;
+  }
+  const int n_ent = n_uniq + ns;
+  if (lane == 0) ent_offset[n_ent] = nvalid + ns * T;
+  __syncwarp();
+  __threadfence_block();
+  // work items per entry, exclusive prefix over entries (warp scan in chunks)
+  int na_run = 0, nb_run = 0, bt_run = 0;
+  for (int base = 0; base < n_ent; base += 32) {
+    const int u = base + lane;
+    int ia = 0, ib = 0, ntg = 0;
+    if (u < n_ent) {
+      const int cu = ent_count[u];
+      const int iu = u < n_uniq ? c.inter : c.shared_inter;
+      ntg = (cu + TG - 1) / TG;
+      ia = (iu / RA) * ntg;
+      ib = (H / RB) * ntg;
+    }
+    int sa = ia, sb = ib, st = ntg;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int na = __shfl_up_sync(0xffffffffu, sa, o), nbv = __shfl_up_sync(0xffffffffu, sb, o),
+                nt = __shfl_up_sync(0xffffffffu, st, o);
+      if (lane >= o) { sa += na; sb += nbv; st += nt; }
+    }
+    if (u < n_ent) {
+      ent_item_a[u] = na_run + sa - ia;
+      ent_item_b[u] = nb_run + sb - ib;
+    }
+    na_run += __shfl_sync(0xffffffffu, sa, 31);
+    nb_run += __shfl_sync(0xffffffffu, sb, 31);
+    bt_run += __shfl_sync(0xffffffffu, st, 31);
+  }
+  if (lane == 0) {
+    ent_item_a[n_ent] = na_run;
+    ent_item_b[n_ent] = nb_run;
+    hdr[H_NENT] = n_ent;
+    hdr[H_NUNIQ] = n_uniq;
+    hdr[H_NA] = na_run;
+    hdr[H_NB] = nb_run;
+    hdr[H_BTARGET] = bt_run;
+    hdr[H_NPAIRS] = nvalid + ns * T;
+  }
+}
+
 cudaError_t launch_prep(const PrepParams& P, unsigned grid, size_t smem, cudaStream_t st) {
   cudaError_t e;
   if (P.cfg.weight_bits == 4) {
@@ -237,6 +396,20 @@ cudaError_t launch_prep(const PrepParams& P, unsigned grid, size_t smem, cudaStr
     prep_kernel<8><<<grid, PREP_THREADS, smem, st>>>(P);
   }
   return cudaGetLastError();
+}
+
+cudaError_t launch_prep_small(const PrepParams& P, unsigned grid, cudaStream_t st) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(256);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (P.cfg.weight_bits == 4) return cudaLaunchKernelEx(&cfg, prep_small_kernel<4>, P);
+  return cudaLaunchKernelEx(&cfg, prep_small_kernel<8>, P);
 }
 
 cudaError_t launch_quantize_act(const float* x, long long nblk, int8_t* q, float* d, unsigned blocks,

@@ -6,44 +6,6 @@
 
 namespace colimoe {
 
-// Logits for T <= 8 positions: one warp per (expert, K split), lanes stride
-// float4 columns, partial sums to part[split][t][e] (summed in fixed order by
-// the selection kernel, so results do not depend on scheduling).
-__global__ void __launch_bounds__(256) route_logits_gemv(const float* __restrict__ x, int T, int H,
-                                                         const float* __restrict__ wr, int E,
-                                                         int splits, float* __restrict__ part) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int e = blockIdx.x * 8 + warp;
-  const int s = blockIdx.y;
-  if (e >= E) return;
-  const int n4 = H / 4 / splits;
-  const float4* w4 = reinterpret_cast<const float4*>(wr + (size_t)e * H) + (size_t)s * n4;
-  float acc[ROUTE_GEMV_MAX_T];
-#pragma unroll
-  for (int t = 0; t < ROUTE_GEMV_MAX_T; ++t) acc[t] = 0.f;
-#pragma unroll 6
-  for (int i = lane; i < n4; i += 32) {
-    float4 w = __ldg(w4 + i);
-#pragma unroll
-    for (int t = 0; t < ROUTE_GEMV_MAX_T; ++t) {
-      if (t < T) {
-        float4 v = __ldg(reinterpret_cast<const float4*>(x + (size_t)t * H) + (size_t)s * n4 + i);
-        acc[t] = fmaf(w.x, v.x, acc[t]);
-        acc[t] = fmaf(w.y, v.y, acc[t]);
-        acc[t] = fmaf(w.z, v.z, acc[t]);
-        acc[t] = fmaf(w.w, v.w, acc[t]);
-      }
-    }
-  }
-#pragma unroll
-  for (int t = 0; t < ROUTE_GEMV_MAX_T; ++t) {
-    if (t < T) {
-      float v = warp_sum(acc[t]);
-      if (lane == 0) part[((size_t)s * T + t) * E + e] = v;
-    }
-  }
-}
-
 // Logits for larger T: 64x64 output tiles, K steps of 16, 4x4 per thread.
 __global__ void __launch_bounds__(256) route_logits_tiled(const float* __restrict__ x, int T, int H,
                                                           const float* __restrict__ wr, int E,
@@ -110,26 +72,21 @@ __device__ __forceinline__ ArgMax warp_argmax(ArgMax a) {
 // One warp per position: sigmoid, biased ranking score, group scores (sum
 // of the two best scores of each group), keep topk_group groups, top-k among
 // their experts (descending score, lower id on ties), weights from the
-// unbiased affinities renormalised and scaled.
-__global__ void __launch_bounds__(256) route_select(const float* __restrict__ part, int splits, int T,
-                                                   int E, int G, int topk_group, int k, float rsf,
-                                                   const float* __restrict__ bias,
-                                                   int32_t* __restrict__ topk_idx,
-                                                   float* __restrict__ topk_w,
-                                                   uint32_t* __restrict__ status) {
-  extern __shared__ float sm_sel[];
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int t = blockIdx.x * 8 + warp;
-  if (t >= T) return;
-  float* s_aff = sm_sel + (size_t)warp * 2 * E;
-  float* s_c = s_aff + E;
+// unbiased affinities renormalised and scaled.  `scratch` holds 2*E floats.
+__device__ void select_position(const float* __restrict__ part, int splits, int T, int t, int E, int G,
+                                int topk_group, int k, float rsf, const float* __restrict__ bias,
+                                int32_t* __restrict__ topk_idx, float* __restrict__ topk_w,
+                                uint32_t* __restrict__ status, float* scratch) {
+  const int lane = threadIdx.x & 31;
+  float* s_aff = scratch;
+  float* s_c = scratch + E;
   bool bad = false;
   for (int e = lane; e < E; e += 32) {
     float l = 0.f;
-    for (int s = 0; s < splits; ++s) l += part[((size_t)s * T + t) * E + e];
-    float b = bias[e];
+    for (int s = 0; s < splits; ++s) l += __ldcg(part + ((size_t)s * T + t) * E + e);
+    const float b = bias[e];
     if (!isfinite(l) || !isfinite(b)) bad = true;
-    float sv = __fdiv_rn(1.0f, 1.0f + expf(-l));
+    const float sv = __fdiv_rn(1.0f, 1.0f + expf(-l));
     s_aff[e] = sv;
     s_c[e] = sv + b;
   }
@@ -147,7 +104,7 @@ __global__ void __launch_bounds__(256) route_select(const float* __restrict__ pa
   if (lane < G) {
     float b1 = -INFINITY, b2 = -INFINITY;
     for (int i = 0; i < gsz; ++i) {
-      float v = s_c[lane * gsz + i];
+      const float v = s_c[lane * gsz + i];
       if (v > b1) { b2 = b1; b1 = v; } else if (v > b2) { b2 = v; }
     }
     gscore = gsz >= 2 ? b1 + b2 : b1;
@@ -164,7 +121,7 @@ __global__ void __launch_bounds__(256) route_select(const float* __restrict__ pa
     ArgMax best{-INFINITY, 1 << 20};
     for (int e = lane; e < E; e += 32) {
       if (!((keptmask >> (e / gsz)) & 1u)) continue;
-      float v = s_c[e];
+      const float v = s_c[e];
       if (v == -INFINITY) continue;  // already selected
       best = better(best, ArgMax{v, e});
     }
@@ -173,34 +130,124 @@ __global__ void __launch_bounds__(256) route_select(const float* __restrict__ pa
     if (best.i < E && lane == (best.i & 31)) s_c[best.i] = -INFINITY;
     __syncwarp();
   }
-  float my_s = (lane < k && my_sel >= 0 && my_sel < E) ? s_aff[my_sel] : 0.f;
-  float tot = warp_sum(my_s);
+  const float my_s = (lane < k && my_sel >= 0 && my_sel < E) ? s_aff[my_sel] : 0.f;
+  const float tot = warp_sum(my_s);
   if (lane < k) {
     topk_idx[(size_t)t * k + lane] = my_sel;
     topk_w[(size_t)t * k + lane] = tot > 0.f ? __fmul_rn(__fdiv_rn(my_s, tot), rsf) : 0.f;
   }
 }
 
+__global__ void __launch_bounds__(256) route_select(const float* __restrict__ part, int splits, int T,
+                                                   int E, int G, int topk_group, int k, float rsf,
+                                                   const float* __restrict__ bias,
+                                                   int32_t* __restrict__ topk_idx,
+                                                   float* __restrict__ topk_w,
+                                                   uint32_t* __restrict__ status) {
+  extern __shared__ float sm_sel[];
+  const int warp = threadIdx.x >> 5;
+  const int t = blockIdx.x * 8 + warp;
+  if (t >= T) return;
+  select_position(part, splits, T, t, E, G, topk_group, k, rsf, bias, topk_idx, topk_w, status,
+                  sm_sel + (size_t)warp * 2 * E);
+}
+
+__device__ __forceinline__ void pdl_wait_r() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger_r() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// Router for T <= 8 in one launch: every CTA writes partial logits for 8
+// experts x one K split; the last CTA to finish (a counter in the workspace
+// header, reset by that CTA) runs the selection, one warp per position.
+__global__ void __launch_bounds__(256) route_fused(const float* __restrict__ x, int T, int H,
+                                                  const float* __restrict__ wr, int E, int splits,
+                                                  float* __restrict__ part, int G, int topk_group, int k,
+                                                  float rsf, const float* __restrict__ bias,
+                                                  int32_t* __restrict__ topk_idx, float* __restrict__ topk_w,
+                                                  uint32_t* __restrict__ status, uint32_t* __restrict__ counter) {
+  extern __shared__ float sm_rf[];
+  __shared__ uint32_t s_last;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int e = blockIdx.x * 8 + warp;
+  const int s = blockIdx.y;
+  if (e < E) {
+    const int n4 = H / 4 / splits;
+    const float4* w4 = reinterpret_cast<const float4*>(wr + (size_t)e * H) + (size_t)s * n4;
+    float acc[ROUTE_GEMV_MAX_T];
+#pragma unroll
+    for (int t = 0; t < ROUTE_GEMV_MAX_T; ++t) acc[t] = 0.f;
+#pragma unroll 6
+    for (int i = lane; i < n4; i += 32) {
+      const float4 w = __ldg(w4 + i);
+#pragma unroll
+      for (int t = 0; t < ROUTE_GEMV_MAX_T; ++t) {
+        if (t < T) {
+          const float4 v = __ldg(reinterpret_cast<const float4*>(x + (size_t)t * H) + (size_t)s * n4 + i);
+          acc[t] = fmaf(w.x, v.x, acc[t]);
+          acc[t] = fmaf(w.y, v.y, acc[t]);
+          acc[t] = fmaf(w.z, v.z, acc[t]);
+          acc[t] = fmaf(w.w, v.w, acc[t]);
+        }
+      }
+    }
+#pragma unroll
+    for (int t = 0; t < ROUTE_GEMV_MAX_T; ++t) {
+      if (t < T) {
+        const float v = warp_sum(acc[t]);
+        if (lane == 0) part[((size_t)s * T + t) * E + e] = v;
+      }
+    }
+  }
+  // outputs may still be read by the previous call's kernels until here
+  pdl_wait_r();
+  pdl_trigger_r();
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    const uint32_t total = gridDim.x * gridDim.y;
+    const uint32_t old = atomicAdd(counter, 1u);
+    s_last = (old == total - 1) ? 1u : 0u;
+    if (s_last) {
+      __threadfence();
+      *counter = 0u;  // ready for the next call
+    }
+  }
+  __syncthreads();
+  if (!s_last) return;
+  if (warp < T)
+    select_position(part, splits, T, warp, E, G, topk_group, k, rsf, bias, topk_idx, topk_w, status,
+                    sm_rf + (size_t)warp * 2 * E);
+}
+
 cudaError_t launch_route(const float* x, int T, int H, const float* wr, int E, int G, int topk_group, int k,
                          float rsf, const float* bias, int32_t* topk_idx, float* topk_w, float* part,
-                         uint32_t* status, cudaStream_t st) {
-  int splits = 1;
+                         uint32_t* status, uint32_t* counter, cudaStream_t st) {
+  const size_t smem = (size_t)8 * 2 * E * sizeof(float);
   if (T <= ROUTE_GEMV_MAX_T) {
-    splits = GEMV_SPLITS;
+    int splits = GEMV_SPLITS;
     while (splits > 1 && (H / 4) % (splits * 32)) splits /= 2;
-    dim3 grid((E + 7) / 8, splits);
-    route_logits_gemv<<<grid, 256, 0, st>>>(x, T, H, wr, E, splits, part);
-  } else {
-    dim3 grid((E + 63) / 64, (T + 63) / 64);
-    route_logits_tiled<<<grid, 256, 0, st>>>(x, T, H, wr, E, part);
+    cudaError_t e = cudaFuncSetAttribute(route_fused, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((E + 7) / 8, splits);
+    cfg.blockDim = dim3(256);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, route_fused, x, T, H, wr, E, splits, part, G, topk_group, k, rsf, bias,
+                              topk_idx, topk_w, status, counter);
   }
+  dim3 grid((E + 63) / 64, (T + 63) / 64);
+  route_logits_tiled<<<grid, 256, 0, st>>>(x, T, H, wr, E, part);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  const size_t smem = (size_t)8 * 2 * E * sizeof(float);
   e = cudaFuncSetAttribute(route_select, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  route_select<<<(T + 7) / 8, 256, smem, st>>>(part, splits, T, E, G, topk_group, k, rsf, bias, topk_idx,
-                                               topk_w, status);
+  route_select<<<(T + 7) / 8, 256, smem, st>>>(part, 1, T, E, G, topk_group, k, rsf, bias, topk_idx, topk_w,
+                                               status);
   return cudaGetLastError();
 }
 
