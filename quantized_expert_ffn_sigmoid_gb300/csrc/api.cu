@@ -76,7 +76,7 @@ int do_dispatch(const coli_moe_cfg& c, const float* x, int T, const int32_t* idx
   PrepParams P{c, x, idx, T, ws, L};
   if (T <= GEMV_MAX_T && T * c.top_k <= GEMV_MAX_T * MAX_TOPK) {
     const int nblk = T * (c.hidden / QB);
-    const unsigned grid = (unsigned)((nblk + 8 * 4 - 1) / (8 * 4));  // ~4 blocks per warp
+    const unsigned grid = (unsigned)((nblk + 7) / 8);  // one 32-block per warp
     return rc_of(launch_prep_small(P, grid > 0 ? grid : 1, st));
   }
   const long long nblk = (long long)T * (c.hidden / QB);

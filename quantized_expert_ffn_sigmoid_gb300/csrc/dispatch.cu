@@ -268,6 +268,7 @@ __global__ void __launch_bounds__(256) prep_small_kernel(PrepParams P) {
 
   __shared__ int key[GEMV_MAX_T * MAX_TOPK];
   __shared__ unsigned char first[GEMV_MAX_T * MAX_TOPK];
+  __shared__ int s_entcnt[GEMV_MAX_T * MAX_TOPK + MAX_SHARED];
   pdl_wait_d();  // routing comes from the router kernel
   pdl_trigger_d();
   uint32_t* ctr = reinterpret_cast<uint32_t*>(ws + L.counters);
@@ -331,11 +332,13 @@ __global__ void __launch_bounds__(256) prep_small_kernel(PrepParams P) {
     ent_expert[ent] = e;
     ent_count[ent] = cnt;
     ent_offset[ent] = off;
+    s_entcnt[ent] = cnt;
   }
   for (int s = lane; s < ns; s += 32) {
     ent_expert[n_uniq + s] = E + s;
     ent_count[n_uniq + s] = T;
     ent_offset[n_uniq + s] = nvalid + s * T;
+    s_entcnt[n_uniq + s] = T;
   }
   for (int i = lane; i < ns * T; i += 32) {
     pair_token[nvalid + i] = i % T;
@@ -344,14 +347,13 @@ __global__ void __launch_bounds__(256) prep_small_kernel(PrepParams P) {
   const int n_ent = n_uniq + ns;
   if (lane == 0) ent_offset[n_ent] = nvalid + ns * T;
   __syncwarp();
-  __threadfence_block();
   // work items per entry, exclusive prefix over entries (warp scan in chunks)
   int na_run = 0, nb_run = 0, bt_run = 0;
   for (int base = 0; base < n_ent; base += 32) {
     const int u = base + lane;
     int ia = 0, ib = 0, ntg = 0;
     if (u < n_ent) {
-      const int cu = ent_count[u];
+      const int cu = s_entcnt[u];
       const int iu = u < n_uniq ? c.inter : c.shared_inter;
       ntg = (cu + TG - 1) / TG;
       ia = (iu / RA) * ntg;

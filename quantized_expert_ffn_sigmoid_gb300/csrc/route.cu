@@ -72,18 +72,115 @@ __device__ __forceinline__ ArgMax warp_argmax(ArgMax a) {
 // One warp per position: sigmoid, biased ranking score, group scores (sum
 // of the two best scores of each group), keep topk_group groups, top-k among
 // their experts (descending score, lower id on ties), weights from the
-// unbiased affinities renormalised and scaled.  `scratch` holds 2*E floats.
-__device__ void select_position(const float* __restrict__ part, int splits, int T, int t, int E, int G,
-                                int topk_group, int k, float rsf, const float* __restrict__ bias,
-                                int32_t* __restrict__ topk_idx, float* __restrict__ topk_w,
-                                uint32_t* __restrict__ status, float* scratch) {
+// unbiased affinities renormalised and scaled.  Lane l holds experts
+// l + 32m (m < MPL) in registers; `scratch` holds E floats.
+template <int MPL>
+__device__ void select_reg(const float* logits, int t, int E, int G, int topk_group, int k, float rsf,
+                           const float* __restrict__ bias, int32_t* __restrict__ topk_idx,
+                           float* __restrict__ topk_w, uint32_t* __restrict__ status, float* scratch) {
+  const int lane = threadIdx.x & 31;
+  float cv[MPL], sv[MPL];
+  bool bad = false;
+#pragma unroll
+  for (int m = 0; m < MPL; ++m) {
+    const int e = lane + 32 * m;
+    if (e < E) {
+      const float l = logits[e];
+      const float b = __ldg(bias + e);
+      bad |= !isfinite(l) || !isfinite(b);
+      sv[m] = __fdiv_rn(1.0f, 1.0f + expf(-l));
+      cv[m] = sv[m] + b;
+      scratch[e] = cv[m];
+    } else {
+      sv[m] = 0.f;
+      cv[m] = -INFINITY;
+    }
+  }
+  if (__any_sync(0xffffffffu, bad)) {
+    if (lane == 0) atomicOr(status, COLI_STATUS_NONFINITE);
+    if (lane < k) {
+      topk_idx[(size_t)t * k + lane] = -1;
+      topk_w[(size_t)t * k + lane] = 0.f;
+    }
+    return;
+  }
+  __syncwarp();
+  const int gsz = E / G;
+  float gscore = -INFINITY;
+  if (lane < G) {
+    float b1 = -INFINITY, b2 = -INFINITY;
+    const float* g = scratch + lane * gsz;
+    if ((gsz & 3) == 0) {
+      for (int i = 0; i < gsz; i += 4) {
+        const float4 v4 = *reinterpret_cast<const float4*>(g + i);
+        const float vv[4] = {v4.x, v4.y, v4.z, v4.w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          if (vv[q] > b1) { b2 = b1; b1 = vv[q]; } else if (vv[q] > b2) { b2 = vv[q]; }
+        }
+      }
+    } else {
+      for (int i = 0; i < gsz; ++i) {
+        const float v = g[i];
+        if (v > b1) { b2 = b1; b1 = v; } else if (v > b2) { b2 = v; }
+      }
+    }
+    gscore = gsz >= 2 ? b1 + b2 : b1;
+  }
+  bool kept = false;
+  for (int r = 0; r < topk_group; ++r) {
+    ArgMax a{(lane < G && !kept) ? gscore : -INFINITY, lane < G ? lane : 1 << 20};
+    a = warp_argmax(a);
+    if (lane == a.i) kept = true;
+  }
+  const unsigned keptmask = __ballot_sync(0xffffffffu, kept);
+#pragma unroll
+  for (int m = 0; m < MPL; ++m) {
+    const int e = lane + 32 * m;
+    if (e < E && !((keptmask >> (e / gsz)) & 1u)) cv[m] = -INFINITY;  // dropped groups
+  }
+  int my_sel = -1;
+  for (int r = 0; r < k; ++r) {
+    ArgMax best{-INFINITY, 1 << 20};
+#pragma unroll
+    for (int m = 0; m < MPL; ++m) best = better(best, ArgMax{cv[m], lane + 32 * m});
+    best = warp_argmax(best);
+    if (lane == r) my_sel = best.i;
+    if ((best.i & 31) == lane) {
+#pragma unroll
+      for (int m = 0; m < MPL; ++m)
+        if (lane + 32 * m == best.i) cv[m] = -INFINITY;
+    }
+  }
+  // affinity of the selected expert held by its owner lane
+  float my_s = 0.f;
+  for (int r = 0; r < k; ++r) {
+    const int e = __shfl_sync(0xffffffffu, my_sel, r);
+    float sown = 0.f;
+#pragma unroll
+    for (int m = 0; m < MPL; ++m)
+      if (lane + 32 * m == e) sown = sv[m];
+    const float se = __shfl_sync(0xffffffffu, sown, e & 31);
+    if (lane == r) my_s = se;
+  }
+  const float tot = warp_sum(my_s);
+  if (lane < k) {
+    topk_idx[(size_t)t * k + lane] = my_sel;
+    topk_w[(size_t)t * k + lane] = tot > 0.f ? __fmul_rn(__fdiv_rn(my_s, tot), rsf) : 0.f;
+  }
+}
+
+// Same selection for E > 256, with the scores in shared memory (2*E floats).
+__device__ __noinline__ void select_smem(const float* logits, int t, int E, int G, int topk_group, int k,
+                                         float rsf, const float* __restrict__ bias,
+                                         int32_t* __restrict__ topk_idx, float* __restrict__ topk_w,
+                                         uint32_t* __restrict__ status, float* scratch) {
   const int lane = threadIdx.x & 31;
   float* s_aff = scratch;
   float* s_c = scratch + E;
   bool bad = false;
   for (int e = lane; e < E; e += 32) {
-    float l = 0.f;
-    for (int s = 0; s < splits; ++s) l += __ldcg(part + ((size_t)s * T + t) * E + e);
+    const float l = logits[e];
     const float b = bias[e];
     if (!isfinite(l) || !isfinite(b)) bad = true;
     const float sv = __fdiv_rn(1.0f, 1.0f + expf(-l));
@@ -138,6 +235,16 @@ __device__ void select_position(const float* __restrict__ part, int splits, int 
   }
 }
 
+__device__ void select_position(const float* logits, int t, int E, int G, int topk_group, int k, float rsf,
+                                const float* __restrict__ bias, int32_t* __restrict__ topk_idx,
+                                float* __restrict__ topk_w, uint32_t* __restrict__ status, float* scratch) {
+  if (E <= 32) select_reg<1>(logits, t, E, G, topk_group, k, rsf, bias, topk_idx, topk_w, status, scratch);
+  else if (E <= 64) select_reg<2>(logits, t, E, G, topk_group, k, rsf, bias, topk_idx, topk_w, status, scratch);
+  else if (E <= 128) select_reg<4>(logits, t, E, G, topk_group, k, rsf, bias, topk_idx, topk_w, status, scratch);
+  else if (E <= 256) select_reg<8>(logits, t, E, G, topk_group, k, rsf, bias, topk_idx, topk_w, status, scratch);
+  else select_smem(logits, t, E, G, topk_group, k, rsf, bias, topk_idx, topk_w, status, scratch);
+}
+
 __global__ void __launch_bounds__(256) route_select(const float* __restrict__ part, int splits, int T,
                                                    int E, int G, int topk_group, int k, float rsf,
                                                    const float* __restrict__ bias,
@@ -148,7 +255,8 @@ __global__ void __launch_bounds__(256) route_select(const float* __restrict__ pa
   const int warp = threadIdx.x >> 5;
   const int t = blockIdx.x * 8 + warp;
   if (t >= T) return;
-  select_position(part, splits, T, t, E, G, topk_group, k, rsf, bias, topk_idx, topk_w, status,
+  (void)splits;
+  select_position(part + (size_t)t * E, t, E, G, topk_group, k, rsf, bias, topk_idx, topk_w, status,
                   sm_sel + (size_t)warp * 2 * E);
 }
 
@@ -213,9 +321,22 @@ __global__ void __launch_bounds__(256) route_fused(const float* __restrict__ x, 
   }
   __syncthreads();
   if (!s_last) return;
+  // logits = sum of the K-split partials in split order, all loads in flight
+  float* s_logit = sm_rf + (size_t)8 * 2 * E;  // [T][E]
+  for (int i = threadIdx.x; i < T * E; i += blockDim.x) {
+    const int t = i / E, e = i % E;
+    float v[GEMV_SPLITS];
+#pragma unroll
+    for (int s = 0; s < GEMV_SPLITS; ++s) v[s] = s < splits ? __ldcg(part + ((size_t)s * T + t) * E + e) : 0.f;
+    float l = 0.f;
+#pragma unroll
+    for (int s = 0; s < GEMV_SPLITS; ++s) if (s < splits) l += v[s];
+    s_logit[i] = l;
+  }
+  __syncthreads();
   if (warp < T)
-    select_position(part, splits, T, warp, E, G, topk_group, k, rsf, bias, topk_idx, topk_w, status,
-                    sm_rf + (size_t)warp * 2 * E);
+    select_position(s_logit + (size_t)warp * E, warp, E, G, topk_group, k, rsf, bias, topk_idx, topk_w,
+                    status, sm_rf + (size_t)warp * 2 * E);
 }
 
 cudaError_t launch_route(const float* x, int T, int H, const float* wr, int E, int G, int topk_group, int k,
@@ -223,14 +344,15 @@ cudaError_t launch_route(const float* x, int T, int H, const float* wr, int E, i
                          uint32_t* status, uint32_t* counter, cudaStream_t st) {
   const size_t smem = (size_t)8 * 2 * E * sizeof(float);
   if (T <= ROUTE_GEMV_MAX_T) {
+    const size_t smem_f = smem + (size_t)T * E * sizeof(float);
     int splits = GEMV_SPLITS;
     while (splits > 1 && (H / 4) % (splits * 32)) splits /= 2;
-    cudaError_t e = cudaFuncSetAttribute(route_fused, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e = cudaFuncSetAttribute(route_fused, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_f);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((E + 7) / 8, splits);
     cfg.blockDim = dim3(256);
-    cfg.dynamicSmemBytes = smem;
+    cfg.dynamicSmemBytes = smem_f;
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
