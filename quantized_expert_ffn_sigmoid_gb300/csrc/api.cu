@@ -14,6 +14,7 @@ cudaError_t launch_prep(const PrepParams& P, unsigned grid, size_t smem, cudaStr
 cudaError_t launch_prep_small(const PrepParams& P, unsigned grid, cudaStream_t st);
 cudaError_t launch_experts(const ExpertParams& P, int grid, size_t smem, cudaStream_t st, bool dump);
 cudaError_t launch_gemv(const ExpertParams& P, int n_sm, cudaStream_t st, bool dump);
+bool gemv_fits(const coli_moe_cfg& c, const Layout& L);
 size_t experts_smem_bytes(const coli_moe_cfg& c, const Layout& L);
 }  // namespace colimoe
 
@@ -100,7 +101,7 @@ int do_experts(const coli_moe_cfg& c, const coli_moe_weights* w, int T, const fl
   P.L = L;
   P.dump_gu = dump_gu;
   P.dump_d = dump_d;
-  if (T <= GEMV_MAX_T) {
+  if (T <= GEMV_MAX_T && gemv_fits(c, L)) {
     // a few positions: stream the weights through the two GEMV kernels
     const int n_sm = sm_count();
     if (n_sm <= 0) return COLI_ECUDA;

@@ -26,8 +26,7 @@ constexpr int MAX_GROUPS = 32;
 constexpr int GEMV_SPLITS = 8;  // K splits of the router GEMV (T <= 8)
 constexpr int ROUTE_GEMV_MAX_T = 8;
 constexpr int PREP_THREADS = 1024;
-constexpr int GEMV_MAX_T = 8;   // calls up to this many positions take the streaming GEMV path
-constexpr int GU_THREADS = 256; // gate/up GEMV: 8 warps, 4 row pairs each (one 32-row tile)
+constexpr int GEMV_MAX_T = 4;   // calls up to this many positions take the streaming GEMV path
 constexpr int DN_ROWS = 16;     // down GEMV: output rows per CTA (4 warps x 4 rows)
 constexpr uint32_t SPIN_LIMIT = 1u << 22;  // bounded waits (about a second or more)
 
