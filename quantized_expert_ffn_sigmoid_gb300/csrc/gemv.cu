@@ -99,9 +99,12 @@ constexpr int GU_SLOTS = 2;
 
 struct GuItem { int tile, ntok, pair0, inter; const uint8_t* rec; const float* sc; };
 
-template <int BITS, bool DUMP>
+// NT: positions per item the code is specialised for (1: decode; the
+// activation blocks of the single position then live in registers).
+template <int BITS, int NT, bool DUMP>
 __global__ void __launch_bounds__(GU_THREADS, 1) gemv_gu_kernel(ExpertParams P) {
   constexpr int CBYTES = BITS == 4 ? 16 : 32;
+  constexpr int RCPL = 8;  // register-resident blocks per lane when NT == 1
   const coli_moe_cfg& c = P.cfg;
   const Layout& L = P.L;
   uint8_t* ws = P.ws;
@@ -166,6 +169,16 @@ __global__ void __launch_bounds__(GU_THREADS, 1) gemv_gu_kernel(ExpertParams P) 
     }
   }
   __syncthreads();
+  uint4 ra0[NT == 1 ? RCPL : 1], ra1[NT == 1 ? RCPL : 1];
+  int rx[NT == 1 ? RCPL : 1];
+  float rd[NT == 1 ? RCPL : 1];
+  if (NT == 1) {
+#pragma unroll
+    for (int m = 0; m < RCPL; ++m) {
+      const int cc = lane + 32 * m;
+      if (cc < nb) { ra0[m] = s_q0[cc]; ra1[m] = s_q1[cc]; rx[m] = s_x[cc]; rd[m] = s_d[cc]; }
+    }
+  }
   const uint64_t pol = policy_evict_first();
   uint32_t* status = reinterpret_cast<uint32_t*>(ws + L.status);
   const int nmine = nA > (int)blockIdx.x ? (nA - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
@@ -218,9 +231,9 @@ __global__ void __launch_bounds__(GU_THREADS, 1) gemv_gu_kernel(ExpertParams P) 
     const GuItem d = decode(blockIdx.x + j * gridDim.x);
     const int ntok = d.ntok;
     float* hbuf = s_h + (j & 1) * RA * TG;
-    int tok[TG];
+    int tok[NT];
 #pragma unroll
-    for (int t = 0; t < TG; ++t) tok[t] = t < ntok ? s_pt[d.pair0 + t] : 0;
+    for (int t = 0; t < NT; ++t) tok[t] = t < ntok ? s_pt[d.pair0 + t] : 0;
     for (int i = 0; i < GU_RPW; ++i) {
       const int seq = j * GU_RPW + i, slot = seq % GU_SLOTS;
       mbar_wait(&bars[warp * GU_SLOTS + slot], (uint32_t)(seq / GU_SLOTS) & 1u, status);
@@ -228,28 +241,50 @@ __global__ void __launch_bounds__(GU_THREADS, 1) gemv_gu_kernel(ExpertParams P) 
       const uint8_t* urow = grow + rb;
       const int rp = warp + GU_NW * i;
       const int row = d.tile * RA + rp;
-      float pg[TG], pu[TG];
+      float pg[NT], pu[NT];
 #pragma unroll
-      for (int t = 0; t < TG; ++t) { pg[t] = 0.f; pu[t] = 0.f; }
-#pragma unroll 2
-      for (int cc = lane; cc < nb; cc += 32) {
-        WBlk<BITS> wg, wu;
-        wg.lds(grow + (size_t)cc * CBYTES);
-        wu.lds(urow + (size_t)cc * CBYTES);
+      for (int t = 0; t < NT; ++t) { pg[t] = 0.f; pu[t] = 0.f; }
+      if (NT == 1 && nb <= 32 * RCPL) {
+        // one position: activation blocks held in registers
 #pragma unroll
-        for (int t = 0; t < TG; ++t) {
-          if (t < ntok) {
-            const uint4 a0 = s_q0[tok[t] * nb + cc], a1 = s_q1[tok[t] * nb + cc];
-            const int corr = s_x[tok[t] * nb + cc];
-            const float dv = s_d[tok[t] * nb + cc];
-            const int ig = wg.dot(a0, a1, corr);
-            const int iu = wu.dot(a0, a1, corr);
-            pg[t] = fmaf(dv, (float)ig, pg[t]);
-            pu[t] = fmaf(dv, (float)iu, pu[t]);
+        for (int m = 0; m < RCPL; ++m) {
+          const int cc = lane + 32 * m;
+          if (cc < nb) {
+            WBlk<BITS> wg, wu;
+            wg.lds(grow + (size_t)cc * CBYTES);
+            wu.lds(urow + (size_t)cc * CBYTES);
+            const int ig = wg.dot(ra0[m], ra1[m], rx[m]);
+            const int iu = wu.dot(ra0[m], ra1[m], rx[m]);
+            pg[0] = fmaf(rd[m], (float)ig, pg[0]);
+            pu[0] = fmaf(rd[m], (float)iu, pu[0]);
             if (DUMP && P.dump_gu) {
-              const size_t pb = (size_t)(d.pair0 + t) * 2 * L.imax;
+              const size_t pb = (size_t)d.pair0 * 2 * L.imax;
               P.dump_gu[(pb + row) * nb + cc] = ig;
               P.dump_gu[(pb + L.imax + row) * nb + cc] = iu;
+            }
+          }
+        }
+      } else {
+#pragma unroll 2
+        for (int cc = lane; cc < nb; cc += 32) {
+          WBlk<BITS> wg, wu;
+          wg.lds(grow + (size_t)cc * CBYTES);
+          wu.lds(urow + (size_t)cc * CBYTES);
+#pragma unroll
+          for (int t = 0; t < NT; ++t) {
+            if (t < ntok) {
+              const uint4 a0 = s_q0[tok[t] * nb + cc], a1 = s_q1[tok[t] * nb + cc];
+              const int corr = s_x[tok[t] * nb + cc];
+              const float dv = s_d[tok[t] * nb + cc];
+              const int ig = wg.dot(a0, a1, corr);
+              const int iu = wu.dot(a0, a1, corr);
+              pg[t] = fmaf(dv, (float)ig, pg[t]);
+              pu[t] = fmaf(dv, (float)iu, pu[t]);
+              if (DUMP && P.dump_gu) {
+                const size_t pb = (size_t)(d.pair0 + t) * 2 * L.imax;
+                P.dump_gu[(pb + row) * nb + cc] = ig;
+                P.dump_gu[(pb + L.imax + row) * nb + cc] = iu;
+              }
             }
           }
         }
@@ -258,7 +293,7 @@ __global__ void __launch_bounds__(GU_THREADS, 1) gemv_gu_kernel(ExpertParams P) 
       __syncwarp();
       if (lane == 0 && seq + GU_SLOTS < total) issue(seq + GU_SLOTS);
 #pragma unroll
-      for (int t = 0; t < TG; ++t) {
+      for (int t = 0; t < NT; ++t) {
         if (t < ntok) {
           const float gs = warp_sum(pg[t]);
           const float us = warp_sum(pu[t]);
@@ -274,8 +309,9 @@ __global__ void __launch_bounds__(GU_THREADS, 1) gemv_gu_kernel(ExpertParams P) 
     // position; warps t < ntok requantise while the others move on (h is
     // double-buffered by item parity)
     __syncthreads();
-    if (warp < ntok) {
-      const int t = warp;
+    const int qw = (warp - j % GU_NW + GU_NW) % GU_NW;  // rotate the requantising warps
+    if (qw < ntok) {
+      const int t = qw;
       float dd;
       bool bad;
       const int qv = q8_0_lane(hbuf[lane * TG + t], &dd, &bad);
@@ -513,6 +549,14 @@ static cudaError_t launch_down(dim3 g, size_t smem, int nslot, cudaStream_t st, 
   return launch_pdl(gemv_down_kernel<BITS, MT, DUMP>, g, dim3(DN_NW * 32), smem, st, P, nslot);
 }
 
+template <int BITS, int NT, bool DUMP>
+static cudaError_t launch_gu(const ExpertParams& P, int n_sm, size_t smem, cudaStream_t st) {
+  cudaError_t e = cudaFuncSetAttribute(gemv_gu_kernel<BITS, NT, DUMP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)smem);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(gemv_gu_kernel<BITS, NT, DUMP>, dim3(n_sm), dim3(GU_THREADS), smem, st, P);
+}
+
 template <int BITS, bool DUMP>
 static cudaError_t launch_gemv_t(const ExpertParams& P, int n_sm, cudaStream_t st) {
   const size_t smem = gu_smem(P.cfg, P.L);
@@ -520,10 +564,8 @@ static cudaError_t launch_gemv_t(const ExpertParams& P, int n_sm, cudaStream_t s
   size_t smem_d;
   dn_plan(P.cfg, P.L, &nslot_d, &smem_d);
   if (nslot_d < 1 || smem > SMEM_CAP) return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(gemv_gu_kernel<BITS, DUMP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)smem);
-  if (e != cudaSuccess) return e;
-  e = launch_pdl(gemv_gu_kernel<BITS, DUMP>, dim3(n_sm), dim3(GU_THREADS), smem, st, P);
+  cudaError_t e = P.L.T == 1 ? launch_gu<BITS, 1, DUMP>(P, n_sm, smem, st)
+                             : launch_gu<BITS, TG, DUMP>(P, n_sm, smem, st);
   if (e != cudaSuccess) return e;
   const dim3 g(P.cfg.hidden / DN_ROWS);
   if (P.L.T == 1) return launch_down<BITS, 1, DUMP>(g, smem_d, nslot_d, st, P);
