@@ -14,6 +14,9 @@ cudaError_t launch_prep(const PrepParams& P, unsigned grid, size_t smem, cudaStr
 cudaError_t launch_prep_small(const PrepParams& P, unsigned grid, cudaStream_t st);
 cudaError_t launch_experts(const ExpertParams& P, int grid, size_t smem, cudaStream_t st, bool dump);
 cudaError_t launch_gemv(const ExpertParams& P, int n_sm, cudaStream_t st, bool dump);
+bool decode_fits(const coli_moe_cfg& c);
+cudaError_t launch_decode(const ExpertParams& P, const float* x, const int32_t* topk_idx, bool from_ws, int n_sm,
+                          cudaStream_t st, bool dump);
 bool gemv_fits(const coli_moe_cfg& c, const Layout& L);
 size_t experts_smem_bytes(const coli_moe_cfg& c, const Layout& L);
 }  // namespace colimoe
@@ -87,8 +90,12 @@ int do_dispatch(const coli_moe_cfg& c, const float* x, int T, const int32_t* idx
   return rc_of(launch_prep(P, (unsigned)(1 + nq), prep_smem(c), st));
 }
 
+// x / idx given: a single-position call runs the fused layer kernel, which
+// builds its own tables; without them the kernels read what coli_moe_dispatch
+// left in the workspace.
 int do_experts(const coli_moe_cfg& c, const coli_moe_weights* w, int T, const float* topk_w, float* y,
-               uint8_t* ws, const Layout& L, cudaStream_t st, int32_t* dump_gu, int32_t* dump_d) {
+               uint8_t* ws, const Layout& L, cudaStream_t st, int32_t* dump_gu, int32_t* dump_d,
+               const float* x = nullptr, const int32_t* idx = nullptr) {
   ExpertParams P{};
   P.cfg = c;
   P.experts = static_cast<const uint8_t*>(w->experts);
@@ -101,6 +108,11 @@ int do_experts(const coli_moe_cfg& c, const coli_moe_weights* w, int T, const fl
   P.L = L;
   P.dump_gu = dump_gu;
   P.dump_d = dump_d;
+  if (T == 1 && decode_fits(c)) {
+    const int n_sm = sm_count();
+    if (n_sm <= 0) return COLI_ECUDA;
+    return rc_of(launch_decode(P, x, idx, x == nullptr, n_sm, st, dump_gu || dump_d));
+  }
   if (T <= GEMV_MAX_T && gemv_fits(c, L)) {
     // a few positions: stream the weights through the two GEMV kernels
     const int n_sm = sm_count();
@@ -217,6 +229,7 @@ int coli_moe_forward(const coli_moe_cfg* cfg, const coli_moe_weights* weights, c
   Layout L;
   if ((rc = check_ws(c, T, ws, ws_bytes, &L))) return rc;
   uint8_t* w8 = static_cast<uint8_t*>(ws);
+  if (T == 1 && decode_fits(c)) return do_experts(c, weights, T, topk_w, y, w8, L, stream, nullptr, nullptr, x, topk_idx);
   if ((rc = do_dispatch(c, x, T, topk_idx, w8, L, stream))) return rc;
   return do_experts(c, weights, T, topk_w, y, w8, L, stream, nullptr, nullptr);
 }
@@ -236,6 +249,7 @@ int coli_moe_forward_dump(const coli_moe_cfg* cfg, const coli_moe_weights* weigh
   Layout L;
   if ((rc = check_ws(c, T, ws, ws_bytes, &L))) return rc;
   uint8_t* w8 = static_cast<uint8_t*>(ws);
+  if (T == 1 && decode_fits(c)) return do_experts(c, weights, T, topk_w, y, w8, L, stream, acc_gu, acc_d, x, topk_idx);
   if ((rc = do_dispatch(c, x, T, topk_idx, w8, L, stream))) return rc;
   return do_experts(c, weights, T, topk_w, y, w8, L, stream, acc_gu, acc_d);
 }

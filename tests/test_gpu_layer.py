@@ -213,3 +213,40 @@ def test_glm_stack_layers_b32(bits, layer):
     counts = g["entry_count"][:-shape.n_shared]
     print("stack layer", layer, "positions", len(keep), "unique", counts.size, "max per expert",
           counts.max(), st)
+
+
+def test_single_position_edge_cases(tiny):
+    """One position per call takes the fused single-position kernel: duplicate
+    ids, skipped slots, bad ids and non-finite input behave as in the
+    multi-position path."""
+    x = synth.token_batch(tiny.shape, 9, 0, range(1))
+    for idx_row, w_row in (([3, 3, -1, 7], [0.5, 0.25, 9.0, 0.25]), ([-1, -1, -1, -1], [0, 0, 0, 0]),
+                           ([15, 0, 15, 15], [0.1, 0.2, 0.3, 0.4])):
+        idx = np.array([idx_row])
+        w = np.array([w_row], np.float32)
+        g = tiny.run(x, route=False, idx=idx, w=w)
+        check_parity(tiny, x, g, idx=idx, w=w.astype(np.float64))
+    g = tiny.run(x, route=False, idx=np.array([[0, 99, 2, 3]]), w=np.full((1, 4), 0.25, np.float32), dump=False)
+    assert g["status"] == cm.STATUS_BADIDX
+    xn = x.copy()
+    xn[0, 5] = np.inf
+    g = tiny.run(xn, dump=False)
+    assert g["status"] & cm.STATUS_NONFINITE
+
+
+def test_dispatch_then_experts_equals_forward(glm):
+    """The split entry points (dispatch, then experts) give the forward's output."""
+    ws = cm.new_workspace(glm.cfg, 1)
+    for p in range(2):
+        x, _, _ = margin_batch(glm.shape, glm.seed, "split", 1, glm.router_w, glm.bias, start=p)
+        xd = torch.from_numpy(x).cuda()
+        idx = torch.empty((1, 8), dtype=torch.int32, device="cuda")
+        w = torch.empty((1, 8), device="cuda")
+        cm.coli_moe_route(glm.cfg, xd, glm.wr_d, glm.bias_d, idx, w, ws)
+        y1 = torch.empty((1, glm.shape.hidden), device="cuda")
+        y2 = torch.empty_like(y1)
+        cm.coli_moe_forward(glm.cfg, glm.W, xd, idx, w, y1, ws)
+        cm.coli_moe_dispatch(glm.cfg, xd, idx, ws)
+        cm.coli_moe_experts(glm.cfg, glm.W, 1, w, y2, ws)
+        assert cm.coli_moe_status(ws) == 0
+        assert torch.equal(y1, y2)
