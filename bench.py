@@ -3,8 +3,9 @@
 Headline workload: the GLM-5.2-shaped MoE layer at decode batch 1 (hidden
 6144, 256 routed experts in 8 groups, topk_group 4, top-8, moe_inter 2048,
 one shared expert, packed int4 per-row-scaled weights, all experts resident
-in HBM); one step = 1000 independent seeded positions, one layer call each
-(router + expert layer through the C ABI), back to back.
+in HBM); one step = 1000 independent seeded positions, one coli_moe_layer
+call each (router and expert layer in one fused launch, through the C ABI),
+back to back.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
 
@@ -12,10 +13,10 @@ in HBM); one step = 1000 independent seeded positions, one layer call each
   K steps replayed from a CUDA graph; L2 is defeated by rotating 8 identical
   copies of the layer's weights (≈39 GB), so consecutive calls never find a
   weight byte in L2.
-* roofline: the expert kernel's algorithmic bytes per launch (9 expert
-  records: 8 routed + the shared one) over its average launch duration,
-  measured with CUDA events on its stream, against the measured HBM copy
-  bandwidth.
+* roofline: the layer kernel's algorithmic bytes per launch (9 expert
+  records: 8 routed + the shared one, plus the fp32 router weights and bias)
+  over its average launch duration, measured with CUDA events on its stream,
+  against the measured HBM copy bandwidth.
 * e2e: the same tokens/s through the public API called per position from
   Python with host buffers: pinned x copied in, y copied out, inside the timed
   region.
@@ -51,6 +52,15 @@ EXPERT_BYTES = synth.GLM.record_bytes() + 4 * synth.GLM.scale_count()   # 18,915
 ROUTER_BYTES = 4 * synth.GLM.n_experts * synth.GLM.hidden + 4 * synth.GLM.n_experts
 DECODE_TOKENS = 1000
 REPLICAS = 8
+# DRAM bytes (read + write) of one layer-kernel launch on this workload, from
+# an ncu capture (dram__bytes_read.sum + dram__bytes_write.sum, one position,
+# cold L2); reported only while the kernel's sources hash to the value the
+# capture was taken on, null otherwise.
+LAYER_KERNEL_SOURCES = ("quantized_expert_ffn_sigmoid_gb300/csrc/decode.cu",
+                        "quantized_expert_ffn_sigmoid_gb300/csrc/select_cta.cuh",
+                        "quantized_expert_ffn_sigmoid_gb300/csrc/gemv_common.cuh",
+                        "quantized_expert_ffn_sigmoid_gb300/csrc/colimoe_internal.cuh")
+LAYER_KERNEL_TRAFFIC = {"bytes": None, "sources_sha256": None}
 WORKLOAD = ("glm_decode_b1: GLM-5.2-shaped MoE layer (H 6144, E 256 in 8 groups, topk_group 4, top-8, "
             "moe_inter 2048, 1 shared expert, int4 per-row scales, rsf 2.5), decode batch 1, "
             "1000 independent seeded positions per step, one layer call each")
@@ -86,6 +96,16 @@ def sum_over_ranks(value: float, world: int, device=None) -> float:
     t = torch.tensor([value], dtype=torch.float64, device=device)
     dist.all_reduce(t, op=dist.ReduceOp.SUM)
     return float(t.item())
+
+
+def layer_kernel_traffic():
+    import hashlib
+    h = hashlib.sha256()
+    for f in LAYER_KERNEL_SOURCES:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    ok = LAYER_KERNEL_TRAFFIC["sources_sha256"] == h.hexdigest()
+    return LAYER_KERNEL_TRAFFIC["bytes"] if ok else None
 
 
 def read_peaks():
@@ -194,17 +214,15 @@ class DecodeBench:
         self.w = torch.empty((self.n, k), dtype=torch.float32, device=device)
         self.y = torch.empty((self.n, self.shape.hidden), dtype=torch.float32, device=device)
         self.ws = cm.new_workspace(self.cfg, 1)
-        self.launches_per_token = 4   # route logits, route select, dispatch, experts
+        self.launches_per_token = 1   # one fused layer kernel (router + experts)
 
     def step(self):
         cm = self.cm
         for i in range(self.n):
             r = i % self.R
             rec = self.rep[r]
-            xi = self.x[i:i + 1]
-            cm.coli_moe_route(self.cfg, xi, rec[4], rec[5], self.idx[i:i + 1], self.w[i:i + 1], self.ws)
-            cm.coli_moe_forward(self.cfg, self.W[r], xi, self.idx[i:i + 1], self.w[i:i + 1],
-                                self.y[i:i + 1], self.ws)
+            cm.coli_moe_layer(self.cfg, self.W[r], self.x[i:i + 1], rec[4], rec[5], self.idx[i:i + 1],
+                              self.w[i:i + 1], self.y[i:i + 1], self.ws)
 
     def capture(self):
         torch = self.torch
@@ -217,8 +235,9 @@ class DecodeBench:
         self.graph = g
 
     def expert_kernel_ms(self, n=None):
-        """Average expert-kernel duration (CUDA events on its stream); the
-        host enqueues everything behind a sleep so launches are back to back."""
+        """Average duration of the layer kernel (the one launch of
+        coli_moe_layer per position), from CUDA events on its stream; the host
+        enqueues everything behind a sleep so that launches run back to back."""
         torch, cm = self.torch, self.cm
         n = n or self.n
         starts = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
@@ -228,11 +247,9 @@ class DecodeBench:
         for i in range(n):
             r = i % self.R
             rec = self.rep[r]
-            xi = self.x[i:i + 1]
-            cm.coli_moe_route(self.cfg, xi, rec[4], rec[5], self.idx[i:i + 1], self.w[i:i + 1], self.ws)
-            cm.coli_moe_dispatch(self.cfg, xi, self.idx[i:i + 1], self.ws)
             starts[i].record()
-            cm.coli_moe_experts(self.cfg, self.W[r], 1, self.w[i:i + 1], self.y[i:i + 1], self.ws)
+            cm.coli_moe_layer(self.cfg, self.W[r], self.x[i:i + 1], rec[4], rec[5], self.idx[i:i + 1],
+                              self.w[i:i + 1], self.y[i:i + 1], self.ws)
             ends[i].record()
         torch.cuda.synchronize()
         d = [s.elapsed_time(e) for s, e in zip(starts, ends)]
@@ -290,7 +307,7 @@ def run_gpu(args):
     # expert kernel alone (roofline of the dominant kernel)
     k_mean, k_med = b.expert_kernel_ms()
     hbm, _, peak_kind = read_peaks()
-    kbytes = 9 * EXPERT_BYTES
+    kbytes = 9 * EXPERT_BYTES + ROUTER_BYTES
     achieved = kbytes / (k_mean / 1e3) / 1e9
 
     # end to end through the public API with host buffers
@@ -315,13 +332,13 @@ def run_gpu(args):
         "config": {"workload": WORKLOAD, "positions_per_call": 1, "positions_per_step": b.n,
                    "l2": f"inputs larger than L2: {b.R} identical weight copies rotated per call "
                          f"({b.R * (256 + 1) * EXPERT_BYTES / 1e9:.1f} GB)",
-                   "launch": "CUDA graph of the per-position C-ABI calls",
+                   "launch": "CUDA graph of the per-position coli_moe_layer calls",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "layer_bytes_per_token": 9 * EXPERT_BYTES + ROUTER_BYTES,
                    "layer_gbs": round(value / world * (9 * EXPERT_BYTES + ROUTER_BYTES) / 1e9, 1)},
-        "roofline": {"bound": "hbm", "kernel": "experts_kernel", "achieved": round(achieved, 1),
+        "roofline": {"bound": "hbm", "kernel": "decode_layer_kernel", "achieved": round(achieved, 1),
                      "peak": hbm, "unit": "GB/s", "frac": round(achieved / hbm, 4),
-                     "peak_source": f"{peak_kind} (HBM copy)", "traffic": args.traffic,
+                     "peak_source": f"{peak_kind} (HBM copy)", "traffic": args.traffic if args.traffic is not None else layer_kernel_traffic(),
                      "bytes_per_launch": kbytes, "launch_ms_mean": round(k_mean, 5),
                      "launch_ms_median": round(k_med, 5)},
         "e2e": {"value": round(e2e_val, 1), "unit": UNIT, "h2d_bytes_per_step": int(b.x.numel() * 4),
@@ -375,8 +392,7 @@ def secondary(device, b):
     def mtp():
         for c in range(calls):
             r = c % b.R
-            cm.coli_moe_route(b.cfg, x[c], wrs[r], bias, idx[c], w[c], ws)
-            cm.coli_moe_forward(b.cfg, b.W[r], x[c], idx[c], w[c], y[c], ws)
+            cm.coli_moe_layer(b.cfg, b.W[r], x[c], wrs[r], bias, idx[c], w[c], y[c], ws)
     ms = time_graph(mtp, 3)
     byt = (uniq + calls) * EXPERT_BYTES + calls * ROUTER_BYTES
     res["glm_mtp_verify_t4"] = {"tokens_per_s": round(4 * calls / (ms / 1e3), 1),
@@ -396,8 +412,7 @@ def secondary(device, b):
     y = torch.empty((T, shape.hidden), dtype=torch.float32, device=device)
 
     def pre():
-        cm.coli_moe_route(b.cfg, xp, wr, bias, idx, w, ws)
-        cm.coli_moe_forward(b.cfg, b.W[0], xp, idx, w, y, ws)
+        cm.coli_moe_layer(b.cfg, b.W[0], xp, wr, bias, idx, w, y, ws)
     ms = time_graph(pre, 2)
     ops = 2.0 * (T * 8 + T) * 3 * shape.inter * shape.hidden
     byt = (256 + 1) * EXPERT_BYTES + ROUTER_BYTES

@@ -29,6 +29,11 @@
  *     into a sticky status word at the start of the workspace and read (and
  *     cleared) with coli_moe_status().
  *   - Calls that share a workspace must be ordered on one stream.
+ *   - Kernels of this library may start while the kernel before them on the
+ *     stream is finishing (programmatic dependent launch).  Before that
+ *     kernel has completed they read only weights (router_w, corr_bias,
+ *     expert records and scales), never x, routing or the workspace, so one
+ *     call's outputs may be the next call's inputs directly.
  */
 #ifndef COLI_MOE_H
 #define COLI_MOE_H
@@ -54,11 +59,14 @@ extern "C" {
 #define COLI_STATUS_BADIDX    2u  /* forward saw an expert id outside [-1, E)    */
 #define COLI_STATUS_TIMEOUT   4u  /* a bounded device wait expired               */
 
-/* Layer shape.  Limits: hidden % 32 == 0, inter % 32 == 0,
- * shared_inter % 32 == 0, hidden % 64 == 0, n_experts <= 1024,
- * n_experts % n_groups == 0, n_groups <= 32, 1 <= topk_group <= n_groups,
+/* Layer shape.  Limits (COLI_EINVAL / COLI_EUNSUPPORTED otherwise):
+ * hidden % 128 == 0, inter % 128 == 0, shared_inter % 128 == 0 when
+ * n_shared > 0, n_experts <= 1024, n_experts % n_groups == 0,
+ * n_groups <= 32, 1 <= topk_group <= n_groups,
  * 1 <= top_k <= topk_group * n_experts / n_groups, top_k <= 32,
- * 0 <= n_shared <= 8, weight_bits in {4, 8}. */
+ * 0 <= n_shared <= 8, weight_bits in {4, 8}; a gate+up row pair of hidden
+ * and four down rows of max(inter, shared_inter) must each fit in 32 KiB
+ * (int4: hidden <= 32768, intermediate sizes <= 16384; int8: half). */
 typedef struct coli_moe_cfg {
     int32_t hidden;                 /* H                                    */
     int32_t n_experts;              /* E routed experts                     */
@@ -144,6 +152,19 @@ int coli_moe_forward(const coli_moe_cfg* cfg, const coli_moe_weights* weights,
                      const float* x, int32_t T,
                      const int32_t* topk_idx, const float* topk_w, float* y,
                      void* ws, size_t ws_bytes, cudaStream_t stream);
+
+/* The whole layer: coli_moe_route followed by coli_moe_forward, with the
+ * same arguments, results and status rules as the two calls (topk_idx and
+ * topk_w are outputs here, and the forward part reads them).  For a single
+ * position (T == 1, packed int4) that fits the fused kernel's shared memory,
+ * the router runs inside the expert-layer kernel: one launch per call, the
+ * shared expert's gate/up rows requested before the routing is known.  The
+ * results are bit-identical to the two separate calls. */
+int coli_moe_layer(const coli_moe_cfg* cfg, const coli_moe_weights* weights,
+                   const float* x, int32_t T,
+                   const float* router_w, const float* corr_bias,
+                   int32_t* topk_idx, float* topk_w, float* y,
+                   void* ws, size_t ws_bytes, cudaStream_t stream);
 
 /* The two launches coli_moe_forward makes, callable separately (e.g. to time
  * the expert kernel alone).  coli_moe_dispatch quantises x and builds the

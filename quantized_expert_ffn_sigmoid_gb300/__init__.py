@@ -29,7 +29,7 @@ EXPORTS = (
     "coli_moe_workspace_size", "coli_moe_workspace_init", "coli_moe_route",
     "coli_moe_quantize_act", "coli_moe_forward", "coli_moe_dispatch", "coli_moe_experts",
     "coli_moe_status", "coli_moe_strerror", "coli_moe_workspace_layout",
-    "coli_moe_forward_dump", "coli_moe_forward_static",
+    "coli_moe_forward_dump", "coli_moe_forward_static", "coli_moe_layer",
 )
 STATIC_WS_BYTES = 16 << 20
 
@@ -78,6 +78,7 @@ def _load():
         "coli_moe_workspace_layout": ([CP, I32, ctypes.POINTER(WsLayout)], ctypes.c_int),
         "coli_moe_forward_dump": ([CP, WP, P, I32, P, P, P, P, S, P, P, P], ctypes.c_int),
         "coli_moe_forward_static": ([CP, WP, P, I32, P, P, P, P], ctypes.c_int),
+        "coli_moe_layer": ([CP, WP, P, I32, P, P, P, P, P, P, S, P], ctypes.c_int),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -161,6 +162,12 @@ def coli_moe_forward(cfg, weights: Weights, x, topk_idx, topk_w, y, ws, stream=N
     _check(lib.coli_moe_forward(ctypes.byref(_cfg(cfg)), ctypes.byref(weights), _ptr(x), x.shape[0],
                                 _ptr(topk_idx), _ptr(topk_w), _ptr(y), _ptr(ws), ws.numel(),
                                 _stream(stream)), "coli_moe_forward")
+
+
+def coli_moe_layer(cfg, weights: Weights, x, router_w, corr_bias, topk_idx, topk_w, y, ws, stream=None):
+    _check(lib.coli_moe_layer(ctypes.byref(_cfg(cfg)), ctypes.byref(weights), _ptr(x), x.shape[0],
+                              _ptr(router_w), _ptr(corr_bias), _ptr(topk_idx), _ptr(topk_w), _ptr(y),
+                              _ptr(ws), ws.numel(), _stream(stream)), "coli_moe_layer")
 
 
 def coli_moe_dispatch(cfg, x, topk_idx, ws, stream=None):

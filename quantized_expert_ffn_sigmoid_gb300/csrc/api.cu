@@ -17,6 +17,9 @@ cudaError_t launch_gemv(const ExpertParams& P, int n_sm, cudaStream_t st, bool d
 bool decode_fits(const coli_moe_cfg& c);
 cudaError_t launch_decode(const ExpertParams& P, const float* x, const int32_t* topk_idx, bool from_ws, int n_sm,
                           cudaStream_t st, bool dump);
+bool decode_route_fits(const coli_moe_cfg& c);
+cudaError_t launch_decode_routed(const ExpertParams& P, const float* x, const float* router_w, const float* bias,
+                                 int32_t* topk_idx, float* topk_w, int n_sm, cudaStream_t st);
 bool gemv_fits(const coli_moe_cfg& c, const Layout& L);
 size_t experts_smem_bytes(const coli_moe_cfg& c, const Layout& L);
 }  // namespace colimoe
@@ -93,9 +96,8 @@ int do_dispatch(const coli_moe_cfg& c, const float* x, int T, const int32_t* idx
 // x / idx given: a single-position call runs the fused layer kernel, which
 // builds its own tables; without them the kernels read what coli_moe_dispatch
 // left in the workspace.
-int do_experts(const coli_moe_cfg& c, const coli_moe_weights* w, int T, const float* topk_w, float* y,
-               uint8_t* ws, const Layout& L, cudaStream_t st, int32_t* dump_gu, int32_t* dump_d,
-               const float* x = nullptr, const int32_t* idx = nullptr) {
+ExpertParams expert_params(const coli_moe_cfg& c, const coli_moe_weights* w, const float* topk_w, float* y,
+                           uint8_t* ws, const Layout& L, int32_t* dump_gu, int32_t* dump_d) {
   ExpertParams P{};
   P.cfg = c;
   P.experts = static_cast<const uint8_t*>(w->experts);
@@ -108,6 +110,13 @@ int do_experts(const coli_moe_cfg& c, const coli_moe_weights* w, int T, const fl
   P.L = L;
   P.dump_gu = dump_gu;
   P.dump_d = dump_d;
+  return P;
+}
+
+int do_experts(const coli_moe_cfg& c, const coli_moe_weights* w, int T, const float* topk_w, float* y,
+               uint8_t* ws, const Layout& L, cudaStream_t st, int32_t* dump_gu, int32_t* dump_d,
+               const float* x = nullptr, const int32_t* idx = nullptr) {
+  const ExpertParams P = expert_params(c, w, topk_w, y, ws, L, dump_gu, dump_d);
   if (T == 1 && decode_fits(c)) {
     const int n_sm = sm_count();
     if (n_sm <= 0) return COLI_ECUDA;
@@ -229,6 +238,38 @@ int coli_moe_forward(const coli_moe_cfg* cfg, const coli_moe_weights* weights, c
   Layout L;
   if ((rc = check_ws(c, T, ws, ws_bytes, &L))) return rc;
   uint8_t* w8 = static_cast<uint8_t*>(ws);
+  if (T == 1 && decode_fits(c)) return do_experts(c, weights, T, topk_w, y, w8, L, stream, nullptr, nullptr, x, topk_idx);
+  if ((rc = do_dispatch(c, x, T, topk_idx, w8, L, stream))) return rc;
+  return do_experts(c, weights, T, topk_w, y, w8, L, stream, nullptr, nullptr);
+}
+
+int coli_moe_layer(const coli_moe_cfg* cfg, const coli_moe_weights* weights, const float* x, int32_t T,
+                   const float* router_w, const float* corr_bias, int32_t* topk_idx, float* topk_w, float* y,
+                   void* ws, size_t ws_bytes, cudaStream_t stream) {
+  int rc = check_cfg(cfg);
+  if (rc) return rc;
+  if (T < 0) return COLI_EINVAL;
+  if (T == 0) return COLI_OK;
+  const coli_moe_cfg c = normalized(cfg);
+  if ((rc = check_weights(c, weights))) return rc;
+  if (!x || !router_w || !corr_bias || !topk_idx || !topk_w || !y) return COLI_EINVAL;
+  if (!aligned16(x) || !aligned16(router_w) || !aligned16(corr_bias) || !aligned16(topk_idx) ||
+      !aligned16(topk_w) || !aligned16(y))
+    return COLI_EALIGN;
+  Layout L;
+  if ((rc = check_ws(c, T, ws, ws_bytes, &L))) return rc;
+  uint8_t* w8 = static_cast<uint8_t*>(ws);
+  if (T == 1 && decode_route_fits(c)) {
+    const int n_sm = sm_count();
+    if (n_sm <= 0) return COLI_ECUDA;
+    const ExpertParams P = expert_params(c, weights, topk_w, y, w8, L, nullptr, nullptr);
+    return rc_of(launch_decode_routed(P, x, router_w, corr_bias, topk_idx, topk_w, n_sm, stream));
+  }
+  rc = rc_of(launch_route(x, T, c.hidden, router_w, c.n_experts, c.n_groups, c.topk_group, c.top_k,
+                          c.routed_scaling_factor, corr_bias, topk_idx, topk_w,
+                          reinterpret_cast<float*>(w8 + L.route_part), reinterpret_cast<uint32_t*>(w8 + L.status),
+                          reinterpret_cast<uint32_t*>(w8 + L.status) + 1, stream));
+  if (rc) return rc;
   if (T == 1 && decode_fits(c)) return do_experts(c, weights, T, topk_w, y, w8, L, stream, nullptr, nullptr, x, topk_idx);
   if ((rc = do_dispatch(c, x, T, topk_idx, w8, L, stream))) return rc;
   return do_experts(c, weights, T, topk_w, y, w8, L, stream, nullptr, nullptr);

@@ -229,10 +229,10 @@ __device__ __forceinline__ void pdl_wait_d() { asm volatile("griddepcontrol.wait
 __device__ __forceinline__ void pdl_trigger_d() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
 // Dispatch for calls of at most GEMV_MAX_T positions (<= 256 pairs): every
-// warp quantises x blocks first (x is an input, so this overlaps the router
-// still finishing), then warp 0 of block 0 waits for the routing and builds
-// the same canonical tables as prep_kernel with warp-level counting (ranks by
-// comparing the <= 256 keys (expert, pair) in shared memory).
+// warp quantises x blocks, then warp 0 of block 0 builds the same canonical
+// tables as prep_kernel with warp-level counting (ranks by comparing the
+// <= 256 keys (expert, pair) in shared memory).  Both x and the routing may
+// come from the kernel this launch overlaps, so everything waits for it.
 template <int BITS>
 __global__ void __launch_bounds__(256) prep_small_kernel(PrepParams P) {
   const coli_moe_cfg& c = P.cfg;
@@ -241,6 +241,8 @@ __global__ void __launch_bounds__(256) prep_small_kernel(PrepParams P) {
   uint32_t* status = reinterpret_cast<uint32_t*>(ws + L.status);
   const int H = c.hidden, E = c.n_experts, k = c.top_k, T = P.T, ns = c.n_shared;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  pdl_wait_d();
+  pdl_trigger_d();
   {
     const int nb = H / QB;
     const int nblk = T * nb;
@@ -269,8 +271,6 @@ __global__ void __launch_bounds__(256) prep_small_kernel(PrepParams P) {
   __shared__ int key[GEMV_MAX_T * MAX_TOPK];
   __shared__ unsigned char first[GEMV_MAX_T * MAX_TOPK];
   __shared__ int s_entcnt[GEMV_MAX_T * MAX_TOPK + MAX_SHARED];
-  pdl_wait_d();  // routing comes from the router kernel
-  pdl_trigger_d();
   uint32_t* ctr = reinterpret_cast<uint32_t*>(ws + L.counters);
   int32_t* hdr = reinterpret_cast<int32_t*>(ws + L.hdr);
   int32_t* ent_expert = reinterpret_cast<int32_t*>(ws + L.ent_expert);

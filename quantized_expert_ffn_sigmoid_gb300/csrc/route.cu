@@ -3,6 +3,7 @@
 // RAM", "How it works (validated core mechanics)"; DeepSeek-V3 group
 // limiting as named on that page).
 #include "colimoe_internal.cuh"
+#include "select_cta.cuh"
 
 namespace colimoe {
 
@@ -265,27 +266,39 @@ __device__ __forceinline__ void pdl_trigger_r() { asm volatile("griddepcontrol.l
 
 // Router for T <= 8 in one launch: every CTA writes partial logits for 8
 // experts x one K split; the last CTA to finish (a counter in the workspace
-// header, reset by that CTA) runs the selection, one warp per position.
+// header, reset by that CTA) sums the splits and runs the CTA-wide selection
+// for each position in turn.
+constexpr int RF_PRE = 8;  // router weight float4 per lane loaded before the dependency wait
+
 __global__ void __launch_bounds__(256) route_fused(const float* __restrict__ x, int T, int H,
                                                   const float* __restrict__ wr, int E, int splits,
                                                   float* __restrict__ part, int G, int topk_group, int k,
                                                   float rsf, const float* __restrict__ bias,
                                                   int32_t* __restrict__ topk_idx, float* __restrict__ topk_w,
                                                   uint32_t* __restrict__ status, uint32_t* __restrict__ counter) {
-  extern __shared__ float sm_rf[];
+  extern __shared__ __align__(16) float sm_rf[];
   __shared__ uint32_t s_last;
+  __shared__ SelShared s_sel;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int e = blockIdx.x * 8 + warp;
   const int s = blockIdx.y;
+  // Weights (router rows, bias) are never written by this library's kernels,
+  // so they are loaded before the grid dependency wait; x may be the output
+  // of the kernel this launch overlaps and is read only after it.
+  const float bias_reg = (int)threadIdx.x < E ? __ldg(bias + threadIdx.x) : 0.f;
+  const int n4 = H / 4 / splits;
+  const float4* w4 = reinterpret_cast<const float4*>(wr + (size_t)(e < E ? e : 0) * H) + (size_t)s * n4;
+  float4 wv[RF_PRE];
+#pragma unroll
+  for (int m = 0; m < RF_PRE; ++m)
+    if (e < E && lane + 32 * m < n4) wv[m] = __ldg(w4 + lane + 32 * m);
+  pdl_wait_r();
+  pdl_trigger_r();
   if (e < E) {
-    const int n4 = H / 4 / splits;
-    const float4* w4 = reinterpret_cast<const float4*>(wr + (size_t)e * H) + (size_t)s * n4;
     float acc[ROUTE_GEMV_MAX_T];
 #pragma unroll
     for (int t = 0; t < ROUTE_GEMV_MAX_T; ++t) acc[t] = 0.f;
-#pragma unroll 6
-    for (int i = lane; i < n4; i += 32) {
-      const float4 w = __ldg(w4 + i);
+    auto fma4 = [&](const float4& w, int i) {
 #pragma unroll
       for (int t = 0; t < ROUTE_GEMV_MAX_T; ++t) {
         if (t < T) {
@@ -296,7 +309,11 @@ __global__ void __launch_bounds__(256) route_fused(const float* __restrict__ x, 
           acc[t] = fmaf(w.w, v.w, acc[t]);
         }
       }
-    }
+    };
+#pragma unroll
+    for (int m = 0; m < RF_PRE; ++m)
+      if (lane + 32 * m < n4) fma4(wv[m], lane + 32 * m);
+    for (int i = lane + 32 * RF_PRE; i < n4; i += 32) fma4(__ldg(w4 + i), i);
 #pragma unroll
     for (int t = 0; t < ROUTE_GEMV_MAX_T; ++t) {
       if (t < T) {
@@ -305,9 +322,6 @@ __global__ void __launch_bounds__(256) route_fused(const float* __restrict__ x, 
       }
     }
   }
-  // outputs may still be read by the previous call's kernels until here
-  pdl_wait_r();
-  pdl_trigger_r();
   __syncthreads();
   if (threadIdx.x == 0) {
     __threadfence();
@@ -322,7 +336,7 @@ __global__ void __launch_bounds__(256) route_fused(const float* __restrict__ x, 
   __syncthreads();
   if (!s_last) return;
   // logits = sum of the K-split partials in split order, all loads in flight
-  float* s_logit = sm_rf + (size_t)8 * 2 * E;  // [T][E]
+  float* s_logit = sm_rf + (size_t)2 * E;  // [T][E]
   for (int i = threadIdx.x; i < T * E; i += blockDim.x) {
     const int t = i / E, e = i % E;
     float v[GEMV_SPLITS];
@@ -334,9 +348,9 @@ __global__ void __launch_bounds__(256) route_fused(const float* __restrict__ x, 
     s_logit[i] = l;
   }
   __syncthreads();
-  if (warp < T)
-    select_position(s_logit + (size_t)warp * E, warp, E, G, topk_group, k, rsf, bias, topk_idx, topk_w,
-                    status, sm_rf + (size_t)warp * 2 * E);
+  for (int t = 0; t < T; ++t)
+    select_cta(s_logit + (size_t)t * E, t, E, G, topk_group, k, rsf, bias, bias_reg, topk_idx, topk_w, status,
+               sm_rf, s_sel, true);
 }
 
 cudaError_t launch_route(const float* x, int T, int H, const float* wr, int E, int G, int topk_group, int k,
@@ -344,7 +358,7 @@ cudaError_t launch_route(const float* x, int T, int H, const float* wr, int E, i
                          uint32_t* status, uint32_t* counter, cudaStream_t st) {
   const size_t smem = (size_t)8 * 2 * E * sizeof(float);
   if (T <= ROUTE_GEMV_MAX_T) {
-    const size_t smem_f = smem + (size_t)T * E * sizeof(float);
+    const size_t smem_f = (size_t)(2 + T) * E * sizeof(float);
     int splits = GEMV_SPLITS;
     while (splits > 1 && (H / 4) % (splits * 32)) splits /= 2;
     cudaError_t e = cudaFuncSetAttribute(route_fused, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_f);

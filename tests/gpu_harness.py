@@ -58,14 +58,19 @@ class DeviceLayer:
         return self._host[key]
 
     # ------------------------------------------------------------------ runs
-    def run(self, x: np.ndarray, dump=True, ws=None, route=True, idx=None, w=None):
-        """Route (unless idx/w given) and forward; returns the GPU observables."""
+    def run(self, x: np.ndarray, dump=True, ws=None, route=True, idx=None, w=None, layer=False):
+        """Route (unless idx/w given) and forward; returns the GPU observables.
+        ``layer``: one coli_moe_layer call (router and experts together)."""
         shape, dev = self.shape, self.dev
         T, k = x.shape[0], shape.top_k
         xd = torch.from_numpy(np.ascontiguousarray(x, np.float32)).to(dev)
         if ws is None:
             ws = cm.new_workspace(self.cfg, T)
-        if route:
+        if layer:
+            idx_d = torch.full((T, k), -7, dtype=torch.int32, device=dev)
+            w_d = torch.full((T, k), -7.0, dtype=torch.float32, device=dev)
+            dump = False
+        elif route:
             idx_d = torch.full((T, k), -7, dtype=torch.int32, device=dev)
             w_d = torch.full((T, k), -7.0, dtype=torch.float32, device=dev)
             cm.coli_moe_route(self.cfg, xd, self.wr_d, self.bias_d, idx_d, w_d, ws)
@@ -77,7 +82,9 @@ class DeviceLayer:
         P = T * k + shape.n_shared * T
         imax = max(shape.inter, shape.shared_inter if shape.n_shared else 0)
         acc_gu = acc_d = None
-        if dump:
+        if layer:
+            cm.coli_moe_layer(self.cfg, self.W, xd, self.wr_d, self.bias_d, idx_d, w_d, y, ws)
+        elif dump:
             acc_gu = torch.zeros((P, 2, imax, shape.hidden // 32), dtype=torch.int32, device=dev)
             acc_d = torch.zeros((P, shape.hidden, imax // 32), dtype=torch.int32, device=dev)
             cm.coli_moe_forward_dump(self.cfg, self.W, xd, idx_d, w_d, y, ws, acc_gu, acc_d)
