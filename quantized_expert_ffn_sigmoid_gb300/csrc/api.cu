@@ -158,7 +158,8 @@ size_t coli_moe_workspace_size(const coli_moe_cfg* cfg, int32_t max_T) {
 int coli_moe_workspace_init(void* ws, size_t ws_bytes, cudaStream_t stream) {
   if (!ws || ws_bytes < 256) return COLI_EINVAL;
   if (!aligned16(ws)) return COLI_EALIGN;
-  return cudaMemsetAsync(ws, 0, 256, stream) == cudaSuccess ? COLI_OK : COLI_ECUDA;
+  const size_t n = ws_bytes < WS_HEADER_BYTES ? ws_bytes : WS_HEADER_BYTES;
+  return cudaMemsetAsync(ws, 0, n, stream) == cudaSuccess ? COLI_OK : COLI_ECUDA;
 }
 
 int coli_moe_route(const coli_moe_cfg* cfg, const float* x, int32_t T, const float* router_w,

@@ -23,6 +23,9 @@ constexpr int MAX_E = 1024;
 constexpr int MAX_TOPK = 32;
 constexpr int MAX_SHARED = 8;
 constexpr int MAX_GROUPS = 32;
+// bytes at the start of a workspace that coli_moe_workspace_init clears:
+// status and counter words, then the router's tagged exchange words
+constexpr size_t WS_HEADER_BYTES = 256 + 8 * (size_t)MAX_E;
 constexpr int GEMV_SPLITS = 8;  // K splits of the router GEMV (T <= 8)
 constexpr int ROUTE_GEMV_MAX_T = 8;
 constexpr int PREP_THREADS = 1024;
@@ -53,7 +56,7 @@ __host__ __device__ inline size_t align_up(size_t v, size_t a) { return (v + a -
 // ---------------------------------------------------------------- layout
 struct Layout {
   int T, P, n_ent_max, n_tiles, imax;
-  size_t status, counters, hdr, ent_expert, ent_count, ent_offset, ent_item_a,
+  size_t status, route_words, counters, hdr, ent_expert, ent_count, ent_offset, ent_item_a,
          ent_item_b, pair_token, pair_j, slot, route_part, qx, dx, xs, qh, dh, hs, o, total;
 };
 // Table header (ints at Layout::hdr)
@@ -73,6 +76,7 @@ __host__ __device__ inline Layout make_layout(const coli_moe_cfg& c, int T) {
   size_t off = 0;
   auto take = [&](size_t bytes) { size_t r = off; off = align_up(off + bytes, 256); return r; };
   L.status = take(256);
+  L.route_words = take(8 * (size_t)MAX_E);  // zeroed by coli_moe_workspace_init with the status words
   L.counters = take(4 * (1 + L.n_ent_max + L.n_tiles));
   L.hdr = take(4 * H_FIELDS);
   L.ent_expert = take(4 * (size_t)L.n_ent_max);
@@ -195,6 +199,19 @@ __device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t* p) {
   uint32_t v;
   asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
   return v;
+}
+__device__ __forceinline__ uint32_t ld_relaxed_u32(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ uint64_t ld_relaxed_u64(const uint64_t* p) {
+  uint64_t v;
+  asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_relaxed_u64(uint64_t* p, uint64_t v) {
+  asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }
 __device__ __forceinline__ void red_release_add(uint32_t* p, uint32_t v) {
   asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");

@@ -13,11 +13,12 @@
 //             builds the tiny dispatch tables itself;
 //   DM_WS     tables and activation codes read from the workspace, where a
 //             dispatch launch left them;
-//   DM_ROUTE  the router is part of the kernel: every warp computes one
-//             (expert, K-split) partial logit, CTAs meet at a grid counter,
-//             and each CTA then runs the CTA-wide selection on the summed
-//             logits itself (identical in every CTA), so no second grid
-//             barrier and no separate router launch are needed.  The shared
+//   DM_ROUTE  the router is part of the kernel: each CTA computes the logits
+//             of a few experts (one warp per (expert, K-split), splits summed
+//             in order in shared memory) and publishes each as one 64-bit
+//             word (value, call tag); every CTA polls the E words, then runs
+//             the CTA-wide selection itself (identical in every CTA), so no
+//             grid barrier and no separate router launch are needed.  The shared
 //             expert's gate/up tiles come first in the work order: their rows
 //             are requested before the grid dependency wait and computed
 //             before the routing is known.
@@ -59,7 +60,8 @@ struct DecodeRoute {
   const float* bias;  // [E] correction bias
   int32_t* idx_out;   // [k] selected experts (written by CTA 0)
   float* w_out;       // [k] routing weights (written by CTA 0)
-  int splits;         // K splits of the logit partials
+  int epc;            // experts per CTA
+  int splits;         // K splits per expert (one warp each), epc * splits <= 16
 };
 
 struct DecodeGeo {
@@ -110,7 +112,8 @@ decode_layer_kernel(ExpertParams P, const float* __restrict__ x, const int32_t* 
   uint32_t* status = reinterpret_cast<uint32_t*>(ws + L.status);
   uint32_t* gu_done = status + 2;
   uint32_t* exit_cnt = status + 3;
-  uint32_t* route_cnt = status + 4;
+  uint32_t* epoch_w = status + 5;  // calls of the routing mode completed on this workspace
+  uint64_t* rwords = reinterpret_cast<uint64_t*>(ws + L.route_words);  // [E] (logit bits, tag)
 
   extern __shared__ __align__(128) uint8_t sm_dk[];
   uint8_t* ring = sm_dk + geo.ring;
@@ -129,6 +132,8 @@ decode_layer_kernel(ExpertParams P, const float* __restrict__ x, const int32_t* 
   __shared__ float s_h[2][RA];
   __shared__ int s_n[4];  // n_ent, n_uniq, npair
   __shared__ SelShared s_sel;
+  __shared__ float s_rpart[DK_NW];
+  __shared__ uint32_t s_epoch;
 
   // Work order of phase 1: the shared experts' tiles, then the routed
   // entries' tiles in entry order (every routed expert has inter rows).
@@ -182,19 +187,20 @@ decode_layer_kernel(ExpertParams P, const float* __restrict__ x, const int32_t* 
 
   // ---------------------------------------------------------- before the dependency wait: weights only
   const int my_sh = n_sh_items > (int)blockIdx.x ? (n_sh_items - 1 - (int)blockIdx.x) / G + 1 : 0;
-  const int nwt = G * DK_NW, gw = blockIdx.x * DK_NW + warp;
+  // router task of this warp: expert blockIdx.x * epc + warp / splits, K split warp % splits
   const int rsplits = MODE == DM_ROUTE ? R.splits : 1;
   const int rn4 = H / 4 / rsplits;
+  const int r_e = MODE == DM_ROUTE ? (int)blockIdx.x * R.epc + warp / rsplits : 0;
+  const bool r_task = MODE == DM_ROUTE && warp < R.epc * rsplits && r_e < E;
+  const float4* r_w4 = reinterpret_cast<const float4*>(R.wr + (size_t)r_e * H) + (size_t)(warp % rsplits) * rn4;
   float4 rwv[DK_RWL];
   float bias_reg = 0.f;
   if (MODE == DM_ROUTE) {
     if (lane == 0) top_up(0, my_sh * DK_RPW);
-    if (gw < E * rsplits) {
-      const float4* w4 = reinterpret_cast<const float4*>(R.wr + (size_t)(gw / rsplits) * H) +
-                         (size_t)(gw % rsplits) * rn4;
+    if (r_task) {
 #pragma unroll
       for (int m = 0; m < DK_RWL; ++m)
-        if (lane + 32 * m < rn4) rwv[m] = __ldg(w4 + lane + 32 * m);
+        if (lane + 32 * m < rn4) rwv[m] = __ldg(r_w4 + lane + 32 * m);
     }
     if (tid < E) bias_reg = __ldg(R.bias + tid);
   }
@@ -203,11 +209,9 @@ decode_layer_kernel(ExpertParams P, const float* __restrict__ x, const int32_t* 
 
   // ---------------------------------------------------------- router partial logits
   if (MODE == DM_ROUTE) {
-    float* part = reinterpret_cast<float*>(ws + L.route_part);  // [splits][E]
-    for (int task = gw; task < E * rsplits; task += nwt) {
-      const int e = task / rsplits, s = task % rsplits;
-      const float4* w4 = reinterpret_cast<const float4*>(R.wr + (size_t)e * H) + (size_t)s * rn4;
-      const float4* x4 = reinterpret_cast<const float4*>(x) + (size_t)s * rn4;
+    if (tid == 0) s_epoch = ld_relaxed_u32(epoch_w);
+    if (r_task) {
+      const float4* x4 = reinterpret_cast<const float4*>(x) + (size_t)(warp % rsplits) * rn4;
       float acc = 0.f;
       auto fma4 = [&](const float4& w, int i) {
         const float4 v = __ldg(x4 + i);
@@ -216,19 +220,22 @@ decode_layer_kernel(ExpertParams P, const float* __restrict__ x, const int32_t* 
         acc = fmaf(w.z, v.z, acc);
         acc = fmaf(w.w, v.w, acc);
       };
-      if (task == gw) {
 #pragma unroll
-        for (int m = 0; m < DK_RWL; ++m)
-          if (lane + 32 * m < rn4) fma4(rwv[m], lane + 32 * m);
-        for (int i = lane + 32 * DK_RWL; i < rn4; i += 32) fma4(__ldg(w4 + i), i);
-      } else {
-        for (int i = lane; i < rn4; i += 32) fma4(__ldg(w4 + i), i);
-      }
+      for (int m = 0; m < DK_RWL; ++m)
+        if (lane + 32 * m < rn4) fma4(rwv[m], lane + 32 * m);
+      for (int i = lane + 32 * DK_RWL; i < rn4; i += 32) fma4(__ldg(r_w4 + i), i);
       acc = warp_sum(acc);
-      if (lane == 0) part[(size_t)s * E + e] = acc;
+      if (lane == 0) s_rpart[warp] = acc;
     }
-    __syncthreads();  // this CTA's partials happen-before the release below
-    if (tid == 0) red_release_add(route_cnt, 1u);
+    __syncthreads();
+    // logit = K-split partials summed in split order, published with this
+    // call's tag in the same 64-bit word (one store, no separate flag)
+    const int e = (int)blockIdx.x * R.epc + tid;
+    if (tid < R.epc && e < E) {
+      float l = 0.f;
+      for (int s = 0; s < rsplits; ++s) l += s_rpart[tid * rsplits + s];
+      st_relaxed_u64(rwords + e, ((uint64_t)(s_epoch + 1u) << 32) | __float_as_uint(l));
+    }
   }
 
   // ---------------------------------------------------------- Q8_0 of x
@@ -380,33 +387,82 @@ decode_layer_kernel(ExpertParams P, const float* __restrict__ x, const int32_t* 
       gu_item(0, my_sh * DK_RPW);
       j0 = 1;
     }
-    if (tid == 0) {
+    // every expert's logit word, once it carries this call's tag (bounded wait)
+    float* s_logit = reinterpret_cast<float*>(dact);
+    const uint32_t tag = s_epoch + 1u;
+    for (int e = tid; e < E; e += DK_THREADS) {
+      uint64_t v = 0;
       bool ok = false;
       for (uint32_t i = 0; i < SPIN_LIMIT; ++i) {
-        if (ld_acquire_u32(route_cnt) >= (uint32_t)G) { ok = true; break; }
-        if (i > 4096) __nanosleep(32);
+        v = ld_relaxed_u64(rwords + e);
+        if ((uint32_t)(v >> 32) == tag) { ok = true; break; }
+        if (i > 64) __nanosleep(64);
       }
       if (!ok) atomicOr(status, COLI_STATUS_TIMEOUT);
+      s_logit[e] = __uint_as_float((uint32_t)v);
     }
     __syncthreads();
-    // logits = sum of the K-split partials in split order
-    float* s_logit = reinterpret_cast<float*>(dact);
-    const float* part = reinterpret_cast<const float*>(ws + L.route_part);
-    for (int e = tid; e < E; e += DK_THREADS) {
-      float l = 0.f;
-      for (int s = 0; s < rsplits; ++s) l += __ldcg(part + (size_t)s * E + e);
-      s_logit[e] = l;
-    }
-    __syncthreads();
-    select_cta(s_logit, 0, E, c.n_groups, c.topk_group, k, c.routed_scaling_factor, R.bias, bias_reg, R.idx_out,
+    select_position_cta(s_logit, 0, E, c.n_groups, c.topk_group, k, c.routed_scaling_factor, R.bias, bias_reg, R.idx_out,
                R.w_out, status, s_logit + E, s_sel, blockIdx.x == 0);
   }
 
   // ---------------------------------------------------------- dispatch tables
-  if (MODE != DM_WS) {
+  if (MODE == DM_ROUTE) {
+    // the router's k ids are distinct and valid (or all -1): the entry and
+    // the pair of slot j sit at the id's position in ascending order
+    int32_t* hdr = reinterpret_cast<int32_t*>(ws + L.hdr);
+    const bool okr = s_sel.sel[0] >= 0;
+    const int nu = okr ? k : 0;
+    if (tid < k) {
+      if (okr) {
+        const int a = s_sel.asc[tid], e = s_sel.sel[tid];
+        e_exp[a] = e;
+        e_cnt[a] = 1;
+        e_off[a] = a;
+        p_j[a] = tid;
+        p_w[a] = s_sel.w[tid];
+        if (blockIdx.x == 0) {
+          reinterpret_cast<int32_t*>(ws + L.ent_expert)[a] = e;
+          reinterpret_cast<int32_t*>(ws + L.ent_count)[a] = 1;
+          reinterpret_cast<int32_t*>(ws + L.ent_offset)[a] = a;
+          reinterpret_cast<int32_t*>(ws + L.pair_token)[a] = 0;
+          reinterpret_cast<int32_t*>(ws + L.pair_j)[a] = tid;
+          reinterpret_cast<int32_t*>(ws + L.slot)[tid] = a;
+        }
+      } else if (blockIdx.x == 0) {
+        reinterpret_cast<int32_t*>(ws + L.slot)[tid] = -1;
+      }
+    }
+    if (tid < ns) {
+      e_exp[nu + tid] = E + tid;
+      e_cnt[nu + tid] = 1;
+      e_off[nu + tid] = nu + tid;
+      p_j[nu + tid] = -1;
+      p_w[nu + tid] = 1.0f;
+      if (blockIdx.x == 0) {
+        reinterpret_cast<int32_t*>(ws + L.ent_expert)[nu + tid] = E + tid;
+        reinterpret_cast<int32_t*>(ws + L.ent_count)[nu + tid] = 1;
+        reinterpret_cast<int32_t*>(ws + L.ent_offset)[nu + tid] = nu + tid;
+        reinterpret_cast<int32_t*>(ws + L.pair_token)[nu + tid] = 0;
+        reinterpret_cast<int32_t*>(ws + L.pair_j)[nu + tid] = -1;
+      }
+    }
+    if (tid == 0) {
+      e_off[nu + ns] = nu + ns;
+      s_n[0] = nu + ns;
+      s_n[1] = nu;
+      s_n[2] = nu + ns;
+      if (blockIdx.x == 0) {
+        reinterpret_cast<int32_t*>(ws + L.ent_offset)[nu + ns] = nu + ns;
+        hdr[H_NENT] = nu + ns;
+        hdr[H_NUNIQ] = nu;
+        hdr[H_NPAIRS] = nu + ns;
+      }
+    }
+  } else if (MODE == DM_IDS) {
     // distinct valid ids ascending, pairs by (id, slot), then shared
     if (warp == DK_NW - 1) {
-      const int e = lane < k ? (MODE == DM_ROUTE ? s_sel.sel[lane] : topk_idx[lane]) : -1;
+      const int e = lane < k ? topk_idx[lane] : -1;
       const bool valid = lane < k && e >= 0 && e < E;
       if (blockIdx.x == 0 && __any_sync(0xffffffffu, lane < k && !valid && e != -1) && lane == 0)
         atomicOr(status, COLI_STATUS_BADIDX);
@@ -428,7 +484,7 @@ decode_layer_kernel(ExpertParams P, const float* __restrict__ x, const int32_t* 
         ent += ((fmask >> i) & 1u) && (ki >> 8) < (key >> 8);
       }
       if (first) { e_exp[ent] = e; e_cnt[ent] = cnt; e_off[ent] = rank; }
-      if (valid) { p_j[rank] = lane; p_w[rank] = MODE == DM_ROUTE ? s_sel.w[lane] : P.topk_w[lane]; }
+      if (valid) { p_j[rank] = lane; p_w[rank] = P.topk_w[lane]; }
       if (lane < ns) {
         e_exp[nu + lane] = E + lane;
         e_cnt[nu + lane] = 1;
@@ -622,7 +678,7 @@ decode_layer_kernel(ExpertParams P, const float* __restrict__ x, const int32_t* 
     const uint32_t old = atom_acq_rel_add(exit_cnt, 1u);
     if (old + 1 == gridDim.x) {
       *gu_done = 0u;
-      *route_cnt = 0u;
+      if (MODE == DM_ROUTE) *epoch_w = *epoch_w + 1u;
       *exit_cnt = 0u;
       __threadfence();
     }
@@ -664,10 +720,14 @@ size_t decode_static_smem() {
   return v;
 }
 
-int decode_router_splits(const coli_moe_cfg& c, int n_sm) {
+// experts per CTA and K splits per expert of the in-kernel router (the
+// same splits as the router kernel where the grid allows, so that both
+// produce bit-identical logits)
+void decode_router_split(const coli_moe_cfg& c, int n_sm, int* epc, int* splits) {
+  *epc = (c.n_experts + n_sm - 1) / n_sm;
   int s = GEMV_SPLITS;
-  while (s > 1 && ((c.hidden / 4) % (s * 32) || c.n_experts * s > n_sm * DK_NW)) s /= 2;
-  return s;
+  while (s > 1 && ((c.hidden / 4) % (s * 32) || *epc * s > DK_NW)) s /= 2;
+  *splits = s;
 }
 }  // namespace
 
@@ -680,10 +740,13 @@ bool decode_fits(const coli_moe_cfg& c) {
 }
 
 bool decode_route_fits(const coli_moe_cfg& c) {
-  // the router's logits and selection scratch (3 E floats) live where the
+  // the router's logits and selection scratch (4 E + 32 words) live where the
   // down phase later stages h
-  return decode_fits(c) && (size_t)3 * c.n_experts * 4 <= decode_geo(c).dact_bytes &&
-         c.n_groups <= MAX_GROUPS;
+  int dev = 0, n_sm = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return false;
+  if (cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n_sm <= 0) return false;
+  return decode_fits(c) && ((size_t)4 * c.n_experts + 32) * 4 <= decode_geo(c).dact_bytes &&
+         c.n_groups <= MAX_GROUPS && (c.n_experts + n_sm - 1) / n_sm <= DK_NW;
 }
 
 cudaError_t launch_decode(const ExpertParams& P, const float* x, const int32_t* topk_idx, bool from_ws, int n_sm,
@@ -701,7 +764,7 @@ cudaError_t launch_decode_routed(const ExpertParams& P, const float* x, const fl
   R.bias = bias;
   R.idx_out = topk_idx;
   R.w_out = topk_w;
-  R.splits = decode_router_splits(P.cfg, n_sm);
+  decode_router_split(P.cfg, n_sm, &R.epc, &R.splits);
   return launch_mode<false, DM_ROUTE>(P, x, nullptr, R, n_sm, st);
 }
 

@@ -336,7 +336,7 @@ __global__ void __launch_bounds__(256) route_fused(const float* __restrict__ x, 
   __syncthreads();
   if (!s_last) return;
   // logits = sum of the K-split partials in split order, all loads in flight
-  float* s_logit = sm_rf + (size_t)2 * E;  // [T][E]
+  float* s_logit = sm_rf + (size_t)3 * E + 32;  // [T][E]
   for (int i = threadIdx.x; i < T * E; i += blockDim.x) {
     const int t = i / E, e = i % E;
     float v[GEMV_SPLITS];
@@ -349,7 +349,7 @@ __global__ void __launch_bounds__(256) route_fused(const float* __restrict__ x, 
   }
   __syncthreads();
   for (int t = 0; t < T; ++t)
-    select_cta(s_logit + (size_t)t * E, t, E, G, topk_group, k, rsf, bias, bias_reg, topk_idx, topk_w, status,
+    select_position_cta(s_logit + (size_t)t * E, t, E, G, topk_group, k, rsf, bias, bias_reg, topk_idx, topk_w, status,
                sm_rf, s_sel, true);
 }
 
@@ -358,7 +358,7 @@ cudaError_t launch_route(const float* x, int T, int H, const float* wr, int E, i
                          uint32_t* status, uint32_t* counter, cudaStream_t st) {
   const size_t smem = (size_t)8 * 2 * E * sizeof(float);
   if (T <= ROUTE_GEMV_MAX_T) {
-    const size_t smem_f = (size_t)(2 + T) * E * sizeof(float);
+    const size_t smem_f = ((size_t)(3 + T) * E + 32) * sizeof(float);
     int splits = GEMV_SPLITS;
     while (splits > 1 && (H / 4) % (splits * 32)) splits /= 2;
     cudaError_t e = cudaFuncSetAttribute(route_fused, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_f);
