@@ -60,7 +60,7 @@ LAYER_KERNEL_SOURCES = ("quantized_expert_ffn_sigmoid_gb300/csrc/decode.cu",
                         "quantized_expert_ffn_sigmoid_gb300/csrc/select_cta.cuh",
                         "quantized_expert_ffn_sigmoid_gb300/csrc/gemv_common.cuh",
                         "quantized_expert_ffn_sigmoid_gb300/csrc/colimoe_internal.cuh")
-LAYER_KERNEL_TRAFFIC = {"bytes": None, "sources_sha256": None}
+LAYER_KERNEL_TRAFFIC = {"bytes": 179766144, "sources_sha256": "f443e71fb43bd5a8a166cc2dbec21575c23deaba85ce316cf805478273b546a1"}
 WORKLOAD = ("glm_decode_b1: GLM-5.2-shaped MoE layer (H 6144, E 256 in 8 groups, topk_group 4, top-8, "
             "moe_inter 2048, 1 shared expert, int4 per-row scales, rsf 2.5), decode batch 1, "
             "1000 independent seeded positions per step, one layer call each")
@@ -340,6 +340,7 @@ def run_gpu(args):
                      "peak": hbm, "unit": "GB/s", "frac": round(achieved / hbm, 4),
                      "peak_source": f"{peak_kind} (HBM copy)", "traffic": args.traffic if args.traffic is not None else layer_kernel_traffic(),
                      "bytes_per_launch": kbytes, "launch_ms_mean": round(k_mean, 5),
+                     "achieved_back_to_back": round(kbytes / (ms_max / args.steps / b.n / 1e3) / 1e9, 1),
                      "launch_ms_median": round(k_med, 5)},
         "e2e": {"value": round(e2e_val, 1), "unit": UNIT, "h2d_bytes_per_step": int(b.x.numel() * 4),
                 "d2h_bytes_per_step": int(b.y.numel() * 4)},
