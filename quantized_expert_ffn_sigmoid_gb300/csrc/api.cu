@@ -21,6 +21,8 @@ bool decode_route_fits(const coli_moe_cfg& c);
 cudaError_t launch_decode_routed(const ExpertParams& P, const float* x, const float* router_w, const float* bias,
                                  int32_t* topk_idx, float* topk_w, int n_sm, cudaStream_t st);
 bool gemv_fits(const coli_moe_cfg& c, const Layout& L);
+bool prefill_fits(const coli_moe_cfg& c, int T);
+cudaError_t launch_prefill(const ExpertParams& P, int T, int n_sm, cudaStream_t st, bool dump);
 size_t experts_smem_bytes(const coli_moe_cfg& c, const Layout& L);
 }  // namespace colimoe
 
@@ -121,6 +123,12 @@ int do_experts(const coli_moe_cfg& c, const coli_moe_weights* w, int T, const fl
     const int n_sm = sm_count();
     if (n_sm <= 0) return COLI_ECUDA;
     return rc_of(launch_decode(P, x, idx, x == nullptr, n_sm, st, dump_gu || dump_d));
+  }
+  if (prefill_fits(c, T)) {
+    // many positions: the expert products on the tensor cores
+    const int n_sm = sm_count();
+    if (n_sm <= 0) return COLI_ECUDA;
+    return rc_of(launch_prefill(P, T, n_sm, st, dump_gu || dump_d));
   }
   if (T <= GEMV_MAX_T && gemv_fits(c, L)) {
     // a few positions: stream the weights through the two GEMV kernels
