@@ -176,6 +176,15 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32
   atomicOr(status, COLI_STATUS_TIMEOUT);
   return false;
 }
+// Bounded wait without sleeping between polls, for tight producer/consumer
+// pipelines: try_wait itself suspends the thread in hardware until the phase
+// completes or a short system time limit passes.
+__device__ __forceinline__ bool mbar_wait_tight(uint64_t* bar, uint32_t parity, uint32_t* status) {
+  for (uint32_t i = 0; i < SPIN_LIMIT; ++i)
+    if (mbar_try_wait(bar, parity)) return true;
+  atomicOr(status, COLI_STATUS_TIMEOUT);
+  return false;
+}
 // 1-D bulk async copy global -> shared, completion counted on `bar`.
 // dst, src 16-byte aligned, bytes a multiple of 16.
 __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar,
