@@ -364,8 +364,9 @@ def cm_status(b):
 
 
 def secondary(device, b):
-    """Other workloads on the same resident experts, one graph replay each:
-    MTP verify (4 positions/call) and prefill (2048 positions/call)."""
+    """Other workloads: MTP verify (4 positions/call) and prefill (2048
+    positions/call) on the decode layer's resident experts, and the 25-layer
+    stack at batch 32 on its own resident layers."""
     import torch
     cm = b.cm
     res = {}
@@ -420,7 +421,87 @@ def secondary(device, b):
     res["glm_prefill_s2048"] = {"tokens_per_s": round(T / (ms / 1e3), 1), "ms_per_call": round(ms, 3),
                                 "int8_tops": round(ops / (ms / 1e3) / 1e12, 2),
                                 "gbs_min_bytes": round(byt / (ms / 1e3) / 1e9, 1)}
+    del xp, ws, idx, w, y
+    res["glm_stack24_mtp1_b32"] = stack_bench(device, b)
     return res
+
+
+def stack_bench(device, b, steps=4):
+    """24 int4 GLM layers + 1 int8 layer resident, decode batch 32, Zipf-skewed
+    correction bias per layer, layer inputs x_{l+1} = x_l + delta_l (seeded,
+    independent of y_l); a step = the 25 layer calls, replayed from a graph."""
+    import torch
+    import synth.gpu as sg
+    cm = b.cm
+    seed = synth.WORKLOADS["glm_stack24_mtp1_b32"][1]
+    T, n_layers = 32, 25
+    t0 = time.time()
+    layers = []
+    for l in range(n_layers):
+        shape = synth.GLM_INT8 if l == 24 else synth.GLM
+        recs, scs = sg.expert_records(shape, seed, l, "routed", shape.n_experts, device)
+        srec, ssc = sg.expert_records(shape, seed, l, "shared", 1, device)
+        wr = torch.from_numpy(synth.router_weight(shape, seed, l)).to(device)
+        bias = torch.from_numpy(synth.zipf_router_bias(shape, seed, l)).to(device)
+        layers.append((shape, cm.Cfg.of(shape), (recs, scs, srec, ssc), cm.make_weights(recs, scs, srec, ssc),
+                       wr, bias))
+    resident = sum(sum(a.numel() * a.element_size() for a in L[2]) for L in layers)
+    # layer inputs of every step: x_0 ~ N(0,1) per sequence, then the seeded residual adds
+    xs = torch.empty((steps, n_layers, T, synth.GLM.hidden), device=device)
+    for st in range(steps):
+        x = sg.token_batch(synth.GLM, seed, ("stack", st), range(T), device)
+        for l in range(n_layers):
+            xs[st, l] = x
+            d = sg.normal_f32(synth.make_key(seed, "residual", st, l), 32 * synth.GLM.hidden, 0.1, device)
+            x = x + d[:T * synth.GLM.hidden].view(T, -1)
+    ws = cm.new_workspace(layers[0][1], T)
+    idx = torch.empty((n_layers, T, 8), dtype=torch.int32, device=device)
+    w = torch.empty((n_layers, T, 8), device=device)
+    y = torch.empty((n_layers, T, synth.GLM.hidden), device=device)
+    torch.cuda.synchronize()
+    log(f"[bench] stack: {resident / 1e9:.1f} GB resident in {time.time() - t0:.1f}s")
+    # unique experts per layer (for the bytes moved), from one pass of step 0
+    L = cm.coli_moe_workspace_layout(layers[0][1], T)
+    uniq = []
+    for l, (shape, cfg, _, W, wr, bias) in enumerate(layers):
+        cm.coli_moe_layer(cfg, W, xs[0, l], wr, bias, idx[l], w[l], y[l], ws)
+        uniq.append(int(ws[L.n_entries:L.n_entries + 4].view(torch.int32).item()) - shape.n_shared)
+    def ebytes(sh):
+        return sh.record_bytes() + 4 * sh.scale_count()
+    byt = sum((u + 1) * ebytes(synth.GLM_INT8 if l == 24 else synth.GLM) for l, u in enumerate(uniq)) \
+        + n_layers * ROUTER_BYTES
+
+    def one(st):
+        for l, (shape, cfg, _, W, wr, bias) in enumerate(layers):
+            cm.coli_moe_layer(cfg, W, xs[st, l], wr, bias, idx[l], w[l], y[l], ws)
+
+    graphs = []
+    for st in range(steps):
+        one(st)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, capture_error_mode="thread_local"):
+            one(st)
+        graphs.append(g)
+    for g in graphs:
+        g.replay()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for g in graphs:
+        g.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    st_code = cm.coli_moe_status(ws)
+    del layers, xs, ws
+    torch.cuda.empty_cache()
+    return {"tokens_per_s": round(T / (ms / 1e3), 1), "ms_per_step": round(ms, 3),
+            "unique_experts_per_layer": round(sum(uniq) / n_layers, 1),
+            "gbs": round(byt / (ms / 1e3) / 1e9, 1), "resident_gb": round(resident / 1e9, 1),
+            "steps": steps, "status": st_code,
+            "note": "25 layer calls per step (24 int4 + 1 int8), step = 32 positions; bytes from step 0's unique experts"}
 
 
 def time_graph(fn, reps):
