@@ -426,6 +426,45 @@ def secondary(device, b):
     return res
 
 
+def prefill_only(args):
+    """--only prefill: the prefill workload alone (no decode replicas), for
+    profiling; --prefill-experts / --prefill-t shrink it to a small case with
+    the same kernels.  Prints one JSON line with the call time."""
+    import dataclasses
+    import torch
+    import synth.gpu as sg
+    import quantized_expert_ffn_sigmoid_gb300 as cm
+    device = torch.device("cuda", 0)
+    shape = dataclasses.replace(synth.GLM, n_experts=args.prefill_experts)
+    seed = synth.WORKLOADS["glm_prefill_s2048"][1]
+    T = args.prefill_t
+    recs, scs = sg.expert_records(shape, seed, 0, "routed", shape.n_experts, device)
+    srec, ssc = sg.expert_records(shape, seed, 0, "shared", 1, device)
+    W = cm.make_weights(recs, scs, srec, ssc)
+    cfg = cm.Cfg.of(shape)
+    xp = sg.token_batch(shape, seed, 0, range(T), device)
+    wr = torch.from_numpy(synth.router_weight(shape, seed)).to(device)
+    bias = torch.from_numpy(synth.zero_router_bias(shape)).to(device)
+    ws = cm.new_workspace(cfg, T)
+    idx = torch.empty((T, shape.top_k), dtype=torch.int32, device=device)
+    w = torch.empty((T, shape.top_k), dtype=torch.float32, device=device)
+    y = torch.empty((T, shape.hidden), dtype=torch.float32, device=device)
+    for _ in range(args.warmup):
+        cm.coli_moe_layer(cfg, W, xp, wr, bias, idx, w, y, ws)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        cm.coli_moe_layer(cfg, W, xp, wr, bias, idx, w, y, ws)
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / args.steps
+    print(json.dumps({"workload": f"prefill: GLM-5.2-shaped layer with {shape.n_experts} routed experts, T={T}",
+                      "ms_per_call": round(ms, 3), "tokens_per_s": round(T / (ms / 1e3), 1),
+                      "status": cm.coli_moe_status(ws)}), flush=True)
+
+
 def stack_bench(device, b, steps=4):
     """24 int4 GLM layers + 1 int8 layer resident, decode batch 32, Zipf-skewed
     correction bias per layer, layer inputs x_{l+1} = x_l + delta_l (seeded,
@@ -613,6 +652,10 @@ def main():
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--no-secondary", dest="secondary", action="store_false")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--only", choices=["prefill"], default=None,
+                    help="time one secondary workload alone (profiling)")
+    ap.add_argument("--prefill-experts", type=int, default=256)
+    ap.add_argument("--prefill-t", type=int, default=2048)
     ap.add_argument("--traffic", type=float, default=None,
                     help="ncu dram bytes per expert-kernel launch, if measured for this build")
     args = ap.parse_args()
@@ -621,6 +664,8 @@ def main():
         args.warmup = 3
     if args.impl == "reference":
         run_reference(args)
+    elif args.only == "prefill":
+        prefill_only(args)
     else:
         run_gpu(args)
 
