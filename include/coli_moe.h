@@ -233,7 +233,7 @@ int coli_moe_forward_dump(const coli_moe_cfg* cfg, const coli_moe_weights* weigh
  * library until the process exits).  It calls no cudaMalloc, cudaFree or
  * other allocating routine.  The caller still passes x, routing and y.
  *   - Limit: the layer's workspace for T positions must fit in
- *     COLI_STATIC_WS_BYTES (16 MiB: the GLM-5.2-shaped layer up to T = 66);
+ *     COLI_STATIC_WS_BYTES (24 MiB: the GLM-5.2-shaped layer up to T = 88);
  *     larger T returns COLI_EWORKSPACE and enqueues nothing.
  *   - The first call on a device looks up the array's device address
  *     (cudaGetSymbolAddress, with that device current) and caches it; make
@@ -243,7 +243,7 @@ int coli_moe_forward_dump(const coli_moe_cfg* cfg, const coli_moe_weights* weigh
  *     wrong results.  Calls ordered on one stream are safe; each call rewrites
  *     every table and counter it reads.
  *   - Device status bits (non-finite input, bad ids) are not reported. */
-#define COLI_STATIC_WS_BYTES (16u << 20)
+#define COLI_STATIC_WS_BYTES (24u << 20)
 int coli_moe_forward_static(const coli_moe_cfg* cfg, const coli_moe_weights* weights,
                             const float* x, int32_t T,
                             const int32_t* topk_idx, const float* topk_w, float* y,

@@ -31,7 +31,7 @@ EXPORTS = (
     "coli_moe_status", "coli_moe_strerror", "coli_moe_workspace_layout",
     "coli_moe_forward_dump", "coli_moe_forward_static", "coli_moe_layer",
 )
-STATIC_WS_BYTES = 16 << 20
+STATIC_WS_BYTES = 24 << 20
 
 
 class Cfg(ctypes.Structure):
@@ -206,7 +206,7 @@ def coli_moe_workspace_layout(cfg, T: int) -> WsLayout:
 
 def coli_moe_forward_static(cfg, weights: Weights, x, topk_idx, topk_w, y, stream=None):
     """coli_moe_forward without a caller workspace: the library's static
-    16 MiB device scratch is used instead (for callers that cannot allocate;
+    24 MiB device scratch is used instead (for callers that cannot allocate;
     calls must not overlap on the GPU)."""
     _check(lib.coli_moe_forward_static(ctypes.byref(_cfg(cfg)), ctypes.byref(weights), _ptr(x), x.shape[0],
                                        _ptr(topk_idx), _ptr(topk_w), _ptr(y), _stream(stream)),

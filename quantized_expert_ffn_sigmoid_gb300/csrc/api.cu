@@ -23,6 +23,8 @@ cudaError_t launch_decode_routed(const ExpertParams& P, const float* x, const fl
 bool gemv_fits(const coli_moe_cfg& c, const Layout& L);
 bool prefill_fits(const coli_moe_cfg& c, int T);
 cudaError_t launch_prefill(const ExpertParams& P, int T, int n_sm, cudaStream_t st, bool dump);
+bool sb_fits(const coli_moe_cfg& c, const Layout& L);
+cudaError_t launch_sb(const ExpertParams& P, int n_sm, cudaStream_t st, bool dump);
 size_t experts_smem_bytes(const coli_moe_cfg& c, const Layout& L);
 }  // namespace colimoe
 
@@ -135,6 +137,12 @@ int do_experts(const coli_moe_cfg& c, const coli_moe_weights* w, int T, const fl
     const int n_sm = sm_count();
     if (n_sm <= 0) return COLI_ECUDA;
     return rc_of(launch_gemv(P, n_sm, st, dump_gu || dump_d));
+  }
+  if (sb_fits(c, L)) {
+    // up to a few dozen positions: weight rows on lanes, K split over warps
+    const int n_sm = sm_count();
+    if (n_sm <= 0) return COLI_ECUDA;
+    return rc_of(launch_sb(P, n_sm, st, dump_gu || dump_d));
   }
   const size_t smem = experts_smem_bytes(c, L);
   int dev_smem = 0, dev = 0;

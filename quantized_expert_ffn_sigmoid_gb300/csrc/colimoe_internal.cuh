@@ -30,10 +30,23 @@ constexpr int GEMV_SPLITS = 8;  // K splits of the router GEMV (T <= 8)
 constexpr int ROUTE_GEMV_MAX_T = 8;
 constexpr int PREP_THREADS = 1024;
 constexpr int GEMV_MAX_T = 4;   // calls up to this many positions take the streaming GEMV path
-constexpr int DN_ROWS = 16;     // down GEMV: output rows per CTA (4 warps x 4 rows)
+constexpr int PF_MIN_T = 64;    // calls with at least this many positions take the tcgen05 path
+
 constexpr uint32_t SPIN_LIMIT = 1u << 22;  // bounded waits (about a second or more)
 
 __host__ __device__ inline int row_bytes(int k, int bits) { return bits == 4 ? k / 2 : k; }
+
+// K ranges of the tiled router GEMM (calls of more than ROUTE_GEMV_MAX_T
+// positions): about 1024 CTAs of 64 x 64 logits, at least 192 K elements
+// each; the partial logits of every range are summed in range order.
+__host__ __device__ inline int route_ksplits(int T, int H, int E) {
+  const int tiles = ((E + 63) / 64) * ((T + 63) / 64);
+  const int kmax = H / 192 > 0 ? H / 192 : 1;
+  int ks = 1024 / tiles;
+  ks = ks < 1 ? 1 : (ks > kmax ? kmax : ks);
+  while (ks > 1 && H % (ks * 16)) --ks;
+  return ks;
+}
 __host__ __device__ inline int pow2_floor(int v) { int p = 1; while (p * 2 <= v) p *= 2; return p; }
 // gate+up rows per ring stage for reduction length H
 __host__ __device__ inline int stage_rows_a(int H, int bits) {
@@ -88,7 +101,7 @@ __host__ __device__ inline Layout make_layout(const coli_moe_cfg& c, int T) {
   L.pair_j = take(4 * (size_t)L.P);
   L.slot = take(4 * (size_t)T * k);
   size_t gemv = (size_t)GEMV_SPLITS * (T < ROUTE_GEMV_MAX_T ? T : ROUTE_GEMV_MAX_T) * E;
-  size_t tiled = (size_t)T * E;
+  size_t tiled = (size_t)route_ksplits(T, H, E) * T * E;
   L.route_part = take(4 * (gemv > tiled ? gemv : tiled));
   L.qx = take((size_t)T * H);
   L.dx = take(4 * (size_t)T * (H / QB));

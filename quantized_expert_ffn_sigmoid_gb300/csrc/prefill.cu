@@ -23,15 +23,13 @@
 //   pf_gemm<DN> down tiles of 128 output rows x <= 64 pairs on the Q8_0 h
 //               codes -> fp32 per-pair expert outputs;
 //   pf_combine  y = sum_j w_j o_slot(t,j) + sum_s o_shared, in fixed order.
-#include <cudaTypedefs.h>
-#include "colimoe_internal.cuh"
+#include "tensormap.cuh"
 
 namespace colimoe {
 
 constexpr int PF_M = 128;                   // weight rows per tile (TMEM lanes)
 constexpr int PF_N = 64;                    // pairs per tile
 constexpr uint32_t PF_LBO = 128;            // canonical layout: next 8 K elements
-constexpr int PF_MIN_T = 64;                // calls with at least this many positions
 
 struct PfMaps {
   CUtensorMap w;       // routed records as rows of the gate/up (GU) or down (DN) pitch
@@ -44,12 +42,6 @@ struct PfParams {
   ExpertParams P;
   int T;
 };
-
-__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
-      ::"r"(smem_u32(dst)), "l"(map), "r"(x), "r"(y), "r"(smem_u32(bar)) : "memory");
-}
 
 __device__ __forceinline__ uint64_t umma_desc_s(uint32_t saddr, uint32_t sbo) {
   uint64_t d = (uint64_t)((saddr >> 4) & 0x3FFF);
@@ -599,32 +591,6 @@ __global__ void __launch_bounds__(256) pf_combine(const uint8_t* __restrict__ ws
 
 // ---------------------------------------------------------------- host
 namespace {
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
-        q != cudaDriverEntryPointSuccess)
-      p = nullptr;
-    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  }();
-  return fn;
-}
-
-// rows x row_bytes bytes, boxes of box_rows x box_bytes
-bool encode_rows(CUtensorMap* m, const void* base, size_t row_bytes, size_t rows, uint32_t box_bytes,
-                 uint32_t box_rows) {
-  auto fn = encode_fn();
-  if (!fn || rows == 0) return false;
-  const cuuint64_t dims[2] = {(cuuint64_t)row_bytes, (cuuint64_t)rows};
-  const cuuint64_t strides[1] = {(cuuint64_t)row_bytes};
-  const cuuint32_t box[2] = {box_bytes, box_rows};
-  const cuuint32_t estr[2] = {1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 template <int BITS, bool GU, bool DUMP>
 cudaError_t launch_gemm(const PfMaps& maps, const PfParams& A, size_t smem, int grid, cudaStream_t st) {
   cudaError_t e = cudaFuncSetAttribute(pf_gemm<BITS, GU, DUMP>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);

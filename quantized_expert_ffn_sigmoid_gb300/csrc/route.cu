@@ -7,13 +7,17 @@
 
 namespace colimoe {
 
-// Logits for larger T: 64x64 output tiles, K steps of 16, 4x4 per thread.
+// Logits for larger T: 64x64 output tiles, K steps of 16, 4x4 per thread;
+// blockIdx.z picks one of gridDim.z K ranges of `kper` elements, whose
+// partial logits go to part[z][T][E].  The next step's operands are loaded
+// into registers while the current step is multiplied.
 __global__ void __launch_bounds__(256) route_logits_tiled(const float* __restrict__ x, int T, int H,
                                                           const float* __restrict__ wr, int E,
-                                                          float* __restrict__ part) {
+                                                          float* __restrict__ part, int kper) {
   __shared__ float xs[16][64 + 4];
   __shared__ float ws[16][64 + 4];
   const int t0 = blockIdx.y * 64, e0 = blockIdx.x * 64;
+  const int kb = blockIdx.z * kper, ke = kb + kper;
   const int tid = threadIdx.x;
   const int ty = tid / 16, tx = tid % 16;
   float acc[4][4];
@@ -23,13 +27,22 @@ __global__ void __launch_bounds__(256) route_logits_tiled(const float* __restric
     for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
   // loader: row = tid / 4 (0..63), k4 = tid % 4 (float4 index within 16)
   const int lr = tid / 4, lk = (tid % 4) * 4;
-  for (int k0 = 0; k0 < H; k0 += 16) {
-    float4 xv = make_float4(0.f, 0.f, 0.f, 0.f), wv = xv;
-    if (t0 + lr < T) xv = __ldg(reinterpret_cast<const float4*>(x + (size_t)(t0 + lr) * H + k0 + lk));
-    if (e0 + lr < E) wv = __ldg(reinterpret_cast<const float4*>(wr + (size_t)(e0 + lr) * H + k0 + lk));
+  const float4 zero = make_float4(0.f, 0.f, 0.f, 0.f);
+  auto ldx = [&](int k0) {
+    return t0 + lr < T ? __ldg(reinterpret_cast<const float4*>(x + (size_t)(t0 + lr) * H + k0 + lk)) : zero;
+  };
+  auto ldw = [&](int k0) {
+    return e0 + lr < E ? __ldg(reinterpret_cast<const float4*>(wr + (size_t)(e0 + lr) * H + k0 + lk)) : zero;
+  };
+  float4 xv = ldx(kb), wv = ldw(kb);
+  for (int k0 = kb; k0 < ke; k0 += 16) {
     xs[lk + 0][lr] = xv.x; xs[lk + 1][lr] = xv.y; xs[lk + 2][lr] = xv.z; xs[lk + 3][lr] = xv.w;
     ws[lk + 0][lr] = wv.x; ws[lk + 1][lr] = wv.y; ws[lk + 2][lr] = wv.z; ws[lk + 3][lr] = wv.w;
     __syncthreads();
+    if (k0 + 16 < ke) {
+      xv = ldx(k0 + 16);
+      wv = ldw(k0 + 16);
+    }
 #pragma unroll
     for (int kk = 0; kk < 16; ++kk) {
       float a[4], b[4];
@@ -44,6 +57,7 @@ __global__ void __launch_bounds__(256) route_logits_tiled(const float* __restric
     }
     __syncthreads();
   }
+  float* out = part + (size_t)blockIdx.z * T * E;
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     const int t = t0 + ty * 4 + i;
@@ -51,7 +65,7 @@ __global__ void __launch_bounds__(256) route_logits_tiled(const float* __restric
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       const int e = e0 + tx * 4 + j;
-      if (e < E) part[(size_t)t * E + e] = acc[i][j];
+      if (e < E) out[(size_t)t * E + e] = acc[i][j];
     }
   }
 }
@@ -253,12 +267,18 @@ __global__ void __launch_bounds__(256) route_select(const float* __restrict__ pa
                                                    float* __restrict__ topk_w,
                                                    uint32_t* __restrict__ status) {
   extern __shared__ float sm_sel[];
-  const int warp = threadIdx.x >> 5;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t = blockIdx.x * 8 + warp;
   if (t >= T) return;
-  (void)splits;
-  select_position(part + (size_t)t * E, t, E, G, topk_group, k, rsf, bias, topk_idx, topk_w, status,
-                  sm_sel + (size_t)warp * 2 * E);
+  // logits = the K ranges' partials summed in range order
+  float* lg = sm_sel + (size_t)warp * 3 * E;
+  for (int e = lane; e < E; e += 32) {
+    float l = 0.f;
+    for (int s = 0; s < splits; ++s) l += __ldcg(part + ((size_t)s * T + t) * E + e);
+    lg[e] = l;
+  }
+  __syncwarp();
+  select_position(lg, t, E, G, topk_group, k, rsf, bias, topk_idx, topk_w, status, lg + E);
 }
 
 __device__ __forceinline__ void pdl_wait_r() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
@@ -356,7 +376,7 @@ __global__ void __launch_bounds__(256) route_fused(const float* __restrict__ x, 
 cudaError_t launch_route(const float* x, int T, int H, const float* wr, int E, int G, int topk_group, int k,
                          float rsf, const float* bias, int32_t* topk_idx, float* topk_w, float* part,
                          uint32_t* status, uint32_t* counter, cudaStream_t st) {
-  const size_t smem = (size_t)8 * 2 * E * sizeof(float);
+  const size_t smem = (size_t)8 * 3 * E * sizeof(float);
   if (T <= ROUTE_GEMV_MAX_T) {
     const size_t smem_f = ((size_t)(3 + T) * E + 32) * sizeof(float);
     int splits = GEMV_SPLITS;
@@ -376,13 +396,14 @@ cudaError_t launch_route(const float* x, int T, int H, const float* wr, int E, i
     return cudaLaunchKernelEx(&cfg, route_fused, x, T, H, wr, E, splits, part, G, topk_group, k, rsf, bias,
                               topk_idx, topk_w, status, counter);
   }
-  dim3 grid((E + 63) / 64, (T + 63) / 64);
-  route_logits_tiled<<<grid, 256, 0, st>>>(x, T, H, wr, E, part);
+  const int ks = route_ksplits(T, H, E);
+  dim3 grid((E + 63) / 64, (T + 63) / 64, ks);
+  route_logits_tiled<<<grid, 256, 0, st>>>(x, T, H, wr, E, part, H / ks);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(route_select, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  route_select<<<(T + 7) / 8, 256, smem, st>>>(part, 1, T, E, G, topk_group, k, rsf, bias, topk_idx, topk_w,
+  route_select<<<(T + 7) / 8, 256, smem, st>>>(part, ks, T, E, G, topk_group, k, rsf, bias, topk_idx, topk_w,
                                                status);
   return cudaGetLastError();
 }
