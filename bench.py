@@ -469,6 +469,54 @@ def prefill_only(args):
                       "status": cm.coli_moe_status(ws)}), flush=True)
 
 
+def few_only(args):
+    """--only mtp / --only b32: one workload with a few positions per call, on
+    one resident copy of a GLM-5.2-shaped layer, for profiling.  mtp: the MTP
+    verify chain (4 positions per call); b32: batch 32 with the Zipf-skewed
+    correction bias of the stack's first layer.  Prints one JSON line."""
+    import torch
+    import synth.gpu as sg
+    import quantized_expert_ffn_sigmoid_gb300 as cm
+    device = torch.device("cuda", 0)
+    shape = synth.GLM
+    if args.only == "mtp":
+        seed, T = synth.WORKLOADS["glm_mtp_verify_t4"][1], 4
+        xs = torch.from_numpy(np.stack([synth.mtp_chain(shape, seed, c) for c in range(args.calls)])).to(device)
+        bias = torch.from_numpy(synth.router_bias(shape, seed)).to(device)
+        wr = torch.from_numpy(synth.router_weight(shape, seed)).to(device)
+    else:
+        seed, T = synth.WORKLOADS["glm_stack24_mtp1_b32"][1], 32
+        xs = torch.stack([sg.token_batch(shape, seed, ("b32", c), range(T), device) for c in range(args.calls)])
+        bias = torch.from_numpy(synth.zipf_router_bias(shape, seed, 0)).to(device)
+        wr = torch.from_numpy(synth.router_weight(shape, seed, 0)).to(device)
+    recs, scs = sg.expert_records(shape, seed, 0, "routed", shape.n_experts, device)
+    srec, ssc = sg.expert_records(shape, seed, 0, "shared", 1, device)
+    W = cm.make_weights(recs, scs, srec, ssc)
+    cfg = cm.Cfg.of(shape)
+    ws = cm.new_workspace(cfg, T)
+    idx = torch.empty((args.calls, T, shape.top_k), dtype=torch.int32, device=device)
+    w = torch.empty((args.calls, T, shape.top_k), dtype=torch.float32, device=device)
+    y = torch.empty((args.calls, T, shape.hidden), dtype=torch.float32, device=device)
+
+    def calls():
+        for c in range(args.calls):
+            cm.coli_moe_layer(cfg, W, xs[c], wr, bias, idx[c], w[c], y[c], ws)
+    for _ in range(args.warmup):
+        calls()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        calls()
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / (args.steps * args.calls)
+    print(json.dumps({"workload": f"{args.only}: GLM-5.2-shaped layer, {T} positions per call, {args.calls} calls",
+                      "ms_per_call": round(ms, 4), "tokens_per_s": round(T / (ms / 1e3), 1),
+                      "status": cm.coli_moe_status(ws)}), flush=True)
+
+
 def stack_bench(device, b, steps=4):
     """24 int4 GLM layers + 1 int8 layer resident, decode batch 32, Zipf-skewed
     correction bias per layer, layer inputs x_{l+1} = x_l + delta_l (seeded,
@@ -656,8 +704,9 @@ def main():
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--no-secondary", dest="secondary", action="store_false")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
-    ap.add_argument("--only", choices=["prefill"], default=None,
+    ap.add_argument("--only", choices=["prefill", "mtp", "b32"], default=None,
                     help="time one secondary workload alone (profiling)")
+    ap.add_argument("--calls", type=int, default=20, help="calls per step of --only mtp / b32")
     ap.add_argument("--prefill-experts", type=int, default=256)
     ap.add_argument("--prefill-t", type=int, default=2048)
     ap.add_argument("--traffic", type=float, default=None,
@@ -670,6 +719,8 @@ def main():
         run_reference(args)
     elif args.only == "prefill":
         prefill_only(args)
+    elif args.only in ("mtp", "b32"):
+        few_only(args)
     else:
         run_gpu(args)
 

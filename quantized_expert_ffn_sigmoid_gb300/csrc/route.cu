@@ -70,224 +70,39 @@ __global__ void __launch_bounds__(256) route_logits_tiled(const float* __restric
   }
 }
 
-struct ArgMax { float v; int i; };
-__device__ __forceinline__ ArgMax better(ArgMax a, ArgMax b) {
-  // larger value wins, equal values go to the lower index
-  return (b.v > a.v || (b.v == a.v && b.i < a.i)) ? b : a;
-}
-__device__ __forceinline__ ArgMax warp_argmax(ArgMax a) {
-#pragma unroll
-  for (int o = 16; o; o >>= 1) {
-    ArgMax b{__shfl_xor_sync(0xffffffffu, a.v, o), __shfl_xor_sync(0xffffffffu, a.i, o)};
-    a = better(a, b);
-  }
-  return a;
-}
-
-// One warp per position: sigmoid, biased ranking score, group scores (sum
-// of the two best scores of each group), keep topk_group groups, top-k among
-// their experts (descending score, lower id on ties), weights from the
-// unbiased affinities renormalised and scaled.  Lane l holds experts
-// l + 32m (m < MPL) in registers; `scratch` holds E floats.
-template <int MPL>
-__device__ void select_reg(const float* logits, int t, int E, int G, int topk_group, int k, float rsf,
-                           const float* __restrict__ bias, int32_t* __restrict__ topk_idx,
-                           float* __restrict__ topk_w, uint32_t* __restrict__ status, float* scratch) {
-  const int lane = threadIdx.x & 31;
-  float cv[MPL], sv[MPL];
-  bool bad = false;
-#pragma unroll
-  for (int m = 0; m < MPL; ++m) {
-    const int e = lane + 32 * m;
-    if (e < E) {
-      const float l = logits[e];
-      const float b = __ldg(bias + e);
-      bad |= !isfinite(l) || !isfinite(b);
-      sv[m] = __fdiv_rn(1.0f, 1.0f + expf(-l));
-      cv[m] = sv[m] + b;
-      scratch[e] = cv[m];
-    } else {
-      sv[m] = 0.f;
-      cv[m] = -INFINITY;
-    }
-  }
-  if (__any_sync(0xffffffffu, bad)) {
-    if (lane == 0) atomicOr(status, COLI_STATUS_NONFINITE);
-    if (lane < k) {
-      topk_idx[(size_t)t * k + lane] = -1;
-      topk_w[(size_t)t * k + lane] = 0.f;
-    }
-    return;
-  }
-  __syncwarp();
-  const int gsz = E / G;
-  float gscore = -INFINITY;
-  if (lane < G) {
-    float b1 = -INFINITY, b2 = -INFINITY;
-    const float* g = scratch + lane * gsz;
-    if ((gsz & 3) == 0) {
-      for (int i = 0; i < gsz; i += 4) {
-        const float4 v4 = *reinterpret_cast<const float4*>(g + i);
-        const float vv[4] = {v4.x, v4.y, v4.z, v4.w};
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          if (vv[q] > b1) { b2 = b1; b1 = vv[q]; } else if (vv[q] > b2) { b2 = vv[q]; }
-        }
-      }
-    } else {
-      for (int i = 0; i < gsz; ++i) {
-        const float v = g[i];
-        if (v > b1) { b2 = b1; b1 = v; } else if (v > b2) { b2 = v; }
-      }
-    }
-    gscore = gsz >= 2 ? b1 + b2 : b1;
-  }
-  bool kept = false;
-  for (int r = 0; r < topk_group; ++r) {
-    ArgMax a{(lane < G && !kept) ? gscore : -INFINITY, lane < G ? lane : 1 << 20};
-    a = warp_argmax(a);
-    if (lane == a.i) kept = true;
-  }
-  const unsigned keptmask = __ballot_sync(0xffffffffu, kept);
-#pragma unroll
-  for (int m = 0; m < MPL; ++m) {
-    const int e = lane + 32 * m;
-    if (e < E && !((keptmask >> (e / gsz)) & 1u)) cv[m] = -INFINITY;  // dropped groups
-  }
-  int my_sel = -1;
-  for (int r = 0; r < k; ++r) {
-    ArgMax best{-INFINITY, 1 << 20};
-#pragma unroll
-    for (int m = 0; m < MPL; ++m) best = better(best, ArgMax{cv[m], lane + 32 * m});
-    best = warp_argmax(best);
-    if (lane == r) my_sel = best.i;
-    if ((best.i & 31) == lane) {
-#pragma unroll
-      for (int m = 0; m < MPL; ++m)
-        if (lane + 32 * m == best.i) cv[m] = -INFINITY;
-    }
-  }
-  // affinity of the selected expert held by its owner lane
-  float my_s = 0.f;
-  for (int r = 0; r < k; ++r) {
-    const int e = __shfl_sync(0xffffffffu, my_sel, r);
-    float sown = 0.f;
-#pragma unroll
-    for (int m = 0; m < MPL; ++m)
-      if (lane + 32 * m == e) sown = sv[m];
-    const float se = __shfl_sync(0xffffffffu, sown, e & 31);
-    if (lane == r) my_s = se;
-  }
-  const float tot = warp_sum(my_s);
-  if (lane < k) {
-    topk_idx[(size_t)t * k + lane] = my_sel;
-    topk_w[(size_t)t * k + lane] = tot > 0.f ? __fmul_rn(__fdiv_rn(my_s, tot), rsf) : 0.f;
-  }
-}
-
-// Same selection for E > 256, with the scores in shared memory (2*E floats).
-__device__ __noinline__ void select_smem(const float* logits, int t, int E, int G, int topk_group, int k,
-                                         float rsf, const float* __restrict__ bias,
-                                         int32_t* __restrict__ topk_idx, float* __restrict__ topk_w,
-                                         uint32_t* __restrict__ status, float* scratch) {
-  const int lane = threadIdx.x & 31;
-  float* s_aff = scratch;
-  float* s_c = scratch + E;
-  bool bad = false;
-  for (int e = lane; e < E; e += 32) {
-    const float l = logits[e];
-    const float b = bias[e];
-    if (!isfinite(l) || !isfinite(b)) bad = true;
-    const float sv = __fdiv_rn(1.0f, 1.0f + expf(-l));
-    s_aff[e] = sv;
-    s_c[e] = sv + b;
-  }
-  if (__any_sync(0xffffffffu, bad)) {
-    if (lane == 0) atomicOr(status, COLI_STATUS_NONFINITE);
-    if (lane < k) {
-      topk_idx[(size_t)t * k + lane] = -1;
-      topk_w[(size_t)t * k + lane] = 0.f;
-    }
-    return;
-  }
-  __syncwarp();
-  const int gsz = E / G;
-  float gscore = -INFINITY;
-  if (lane < G) {
-    float b1 = -INFINITY, b2 = -INFINITY;
-    for (int i = 0; i < gsz; ++i) {
-      const float v = s_c[lane * gsz + i];
-      if (v > b1) { b2 = b1; b1 = v; } else if (v > b2) { b2 = v; }
-    }
-    gscore = gsz >= 2 ? b1 + b2 : b1;
-  }
-  bool kept = false;
-  for (int r = 0; r < topk_group; ++r) {
-    ArgMax a{(lane < G && !kept) ? gscore : -INFINITY, lane < G ? lane : 1 << 20};
-    a = warp_argmax(a);
-    if (lane == a.i) kept = true;
-  }
-  const unsigned keptmask = __ballot_sync(0xffffffffu, kept);
-  int my_sel = -1;
-  for (int r = 0; r < k; ++r) {
-    ArgMax best{-INFINITY, 1 << 20};
-    for (int e = lane; e < E; e += 32) {
-      if (!((keptmask >> (e / gsz)) & 1u)) continue;
-      const float v = s_c[e];
-      if (v == -INFINITY) continue;  // already selected
-      best = better(best, ArgMax{v, e});
-    }
-    best = warp_argmax(best);
-    if (lane == r) my_sel = best.i;
-    if (best.i < E && lane == (best.i & 31)) s_c[best.i] = -INFINITY;
-    __syncwarp();
-  }
-  const float my_s = (lane < k && my_sel >= 0 && my_sel < E) ? s_aff[my_sel] : 0.f;
-  const float tot = warp_sum(my_s);
-  if (lane < k) {
-    topk_idx[(size_t)t * k + lane] = my_sel;
-    topk_w[(size_t)t * k + lane] = tot > 0.f ? __fmul_rn(__fdiv_rn(my_s, tot), rsf) : 0.f;
-  }
-}
-
-__device__ void select_position(const float* logits, int t, int E, int G, int topk_group, int k, float rsf,
-                                const float* __restrict__ bias, int32_t* __restrict__ topk_idx,
-                                float* __restrict__ topk_w, uint32_t* __restrict__ status, float* scratch) {
-  if (E <= 32) select_reg<1>(logits, t, E, G, topk_group, k, rsf, bias, topk_idx, topk_w, status, scratch);
-  else if (E <= 64) select_reg<2>(logits, t, E, G, topk_group, k, rsf, bias, topk_idx, topk_w, status, scratch);
-  else if (E <= 128) select_reg<4>(logits, t, E, G, topk_group, k, rsf, bias, topk_idx, topk_w, status, scratch);
-  else if (E <= 256) select_reg<8>(logits, t, E, G, topk_group, k, rsf, bias, topk_idx, topk_w, status, scratch);
-  else select_smem(logits, t, E, G, topk_group, k, rsf, bias, topk_idx, topk_w, status, scratch);
-}
-
+// One CTA per position: the logits are the K ranges' partials summed in range
+// order, then the CTA-wide selection.
 __global__ void __launch_bounds__(256) route_select(const float* __restrict__ part, int splits, int T,
                                                    int E, int G, int topk_group, int k, float rsf,
                                                    const float* __restrict__ bias,
                                                    int32_t* __restrict__ topk_idx,
                                                    float* __restrict__ topk_w,
                                                    uint32_t* __restrict__ status) {
-  extern __shared__ float sm_sel[];
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int t = blockIdx.x * 8 + warp;
-  if (t >= T) return;
-  // logits = the K ranges' partials summed in range order
-  float* lg = sm_sel + (size_t)warp * 3 * E;
-  for (int e = lane; e < E; e += 32) {
+  extern __shared__ __align__(16) float sm_sel[];  // [3E + 32] selection scratch, then [E] logits
+  __shared__ SelShared s_sel;
+  const int t = blockIdx.x;
+  const float bias_reg = (int)threadIdx.x < E ? __ldg(bias + threadIdx.x) : 0.f;
+  asm volatile("griddepcontrol.wait;" ::: "memory");  // the partials come from the previous kernel
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  float* lg = sm_sel + 3 * E + 32;
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
     float l = 0.f;
+#pragma unroll 8
     for (int s = 0; s < splits; ++s) l += __ldcg(part + ((size_t)s * T + t) * E + e);
     lg[e] = l;
   }
-  __syncwarp();
-  select_position(lg, t, E, G, topk_group, k, rsf, bias, topk_idx, topk_w, status, lg + E);
+  __syncthreads();
+  select_position_cta(lg, t, E, G, topk_group, k, rsf, bias, bias_reg, topk_idx, topk_w, status, sm_sel, s_sel, true);
 }
 
 __device__ __forceinline__ void pdl_wait_r() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger_r() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
-// Router for T <= 8 in one launch: every CTA writes partial logits for 8
-// experts x one K split; the last CTA to finish (a counter in the workspace
-// header, reset by that CTA) sums the splits and runs the CTA-wide selection
-// for each position in turn.
+// Router logits for T <= 8: every CTA writes partial logits for 8 experts x
+// one K split.  With one position (fuse_select) the last CTA to finish (a
+// counter in the workspace header, reset by that CTA) sums the splits and
+// runs the CTA-wide selection; with more, route_select (one CTA per
+// position) follows.
 constexpr int RF_PRE = 8;  // router weight float4 per lane loaded before the dependency wait
 
 __global__ void __launch_bounds__(256) route_fused(const float* __restrict__ x, int T, int H,
@@ -295,7 +110,8 @@ __global__ void __launch_bounds__(256) route_fused(const float* __restrict__ x, 
                                                   float* __restrict__ part, int G, int topk_group, int k,
                                                   float rsf, const float* __restrict__ bias,
                                                   int32_t* __restrict__ topk_idx, float* __restrict__ topk_w,
-                                                  uint32_t* __restrict__ status, uint32_t* __restrict__ counter) {
+                                                  uint32_t* __restrict__ status, uint32_t* __restrict__ counter,
+                                                  int fuse_select) {
   extern __shared__ __align__(16) float sm_rf[];
   __shared__ uint32_t s_last;
   __shared__ SelShared s_sel;
@@ -342,6 +158,7 @@ __global__ void __launch_bounds__(256) route_fused(const float* __restrict__ x, 
       }
     }
   }
+  if (!fuse_select) return;  // route_select follows
   __syncthreads();
   if (threadIdx.x == 0) {
     __threadfence();
@@ -373,10 +190,31 @@ __global__ void __launch_bounds__(256) route_fused(const float* __restrict__ x, 
                sm_rf, s_sel, true);
 }
 
+// route_select over `splits` partial-logit ranges, one CTA per position
+// (programmatic dependent launch: it waits for the kernel that wrote them)
+static cudaError_t launch_select(const float* part, int splits, int T, int E, int G, int topk_group, int k,
+                                 float rsf, const float* bias, int32_t* topk_idx, float* topk_w, uint32_t* status,
+                                 cudaStream_t st) {
+  const size_t smem_s = ((size_t)4 * E + 32) * sizeof(float);
+  cudaError_t e = cudaFuncSetAttribute(route_select, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_s);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(T);
+  cfg.blockDim = dim3(256);
+  cfg.dynamicSmemBytes = smem_s;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, route_select, part, splits, T, E, G, topk_group, k, rsf, bias, topk_idx, topk_w,
+                            status);
+}
+
 cudaError_t launch_route(const float* x, int T, int H, const float* wr, int E, int G, int topk_group, int k,
                          float rsf, const float* bias, int32_t* topk_idx, float* topk_w, float* part,
                          uint32_t* status, uint32_t* counter, cudaStream_t st) {
-  const size_t smem = (size_t)8 * 3 * E * sizeof(float);
   if (T <= ROUTE_GEMV_MAX_T) {
     const size_t smem_f = ((size_t)(3 + T) * E + 32) * sizeof(float);
     int splits = GEMV_SPLITS;
@@ -393,19 +231,18 @@ cudaError_t launch_route(const float* x, int T, int H, const float* wr, int E, i
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, route_fused, x, T, H, wr, E, splits, part, G, topk_group, k, rsf, bias,
-                              topk_idx, topk_w, status, counter);
+    // one position: the last CTA selects; more: one CTA per position after
+    e = cudaLaunchKernelEx(&cfg, route_fused, x, T, H, wr, E, splits, part, G, topk_group, k, rsf, bias, topk_idx,
+                           topk_w, status, counter, T == 1 ? 1 : 0);
+    if (e != cudaSuccess || T == 1) return e;
+    return launch_select(part, splits, T, E, G, topk_group, k, rsf, bias, topk_idx, topk_w, status, st);
   }
   const int ks = route_ksplits(T, H, E);
   dim3 grid((E + 63) / 64, (T + 63) / 64, ks);
   route_logits_tiled<<<grid, 256, 0, st>>>(x, T, H, wr, E, part, H / ks);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(route_select, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess) return e;
-  route_select<<<(T + 7) / 8, 256, smem, st>>>(part, ks, T, E, G, topk_group, k, rsf, bias, topk_idx, topk_w,
-                                               status);
-  return cudaGetLastError();
+  return launch_select(part, ks, T, E, G, topk_group, k, rsf, bias, topk_idx, topk_w, status, st);
 }
 
 }  // namespace colimoe
