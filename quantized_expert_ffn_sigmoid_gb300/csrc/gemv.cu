@@ -14,7 +14,7 @@
 //   no-L1-allocate loads, unpacks nibbles in registers and takes dp4a block
 //   dots against the activations held in shared memory.  The 32 h values of
 //   the tile form exactly one Q8_0 block: the CTA requantises them itself.
-// gemv_down: one CTA per SM; each warp owns groups of 2 output rows.  For
+// gemv_down: one CTA per SM; each warp owns groups of 4 output rows.  For
 //   every distinct expert of the call it streams those rows of the down
 //   matrix through a ring of bulk copies and accumulates the
 //   routing-weighted combine in registers, so no per-expert output buffer,
@@ -279,8 +279,20 @@ __global__ void __launch_bounds__(GU_THREADS, 1) gemv_gu_kernel(ExpertParams P) 
 // every pair are copied into shared memory once per CTA by bulk copies; the
 // row scales of each step are prefetched into registers three steps ahead.  The routing-weighted combine accumulates in registers in entry
 // order, so the order of the sum is fixed.
-constexpr int DN_MAX_NW = 24;
-constexpr int DN_R = 2;               // output rows per group (adjacent rows of a down matrix)
+constexpr int DN_MAX_NW = 16;
+constexpr int DN_R = 4;               // output rows per group (adjacent rows of a down matrix)
+// the DN_R row scales of a step as one vector load
+template <int R> struct DnScales;
+template <> struct DnScales<4> {
+  using V = float4;
+  __device__ static V zero() { return make_float4(0.f, 0.f, 0.f, 0.f); }
+  __device__ static void get(const V& v, float* s) { s[0] = v.x; s[1] = v.y; s[2] = v.z; s[3] = v.w; }
+};
+template <> struct DnScales<2> {
+  using V = float2;
+  __device__ static V zero() { return make_float2(0.f, 0.f); }
+  __device__ static void get(const V& v, float* s) { s[0] = v.x; s[1] = v.y; }
+};
 constexpr int DN_SCQ = 3;              // row-scale prefetch depth (steps)
 constexpr uint32_t DN_CHUNK = 32768;   // bytes per staging bulk copy
 
@@ -379,17 +391,17 @@ __global__ void __launch_bounds__(DN_MAX_NW * 32, 1) gemv_down_kernel(ExpertPara
              bar, pol);
   };
   auto row_scales = [&](int q) {   // down scales of the step's 4 rows (every lane)
-    if (q >= dtotal) return make_float2(0.f, 0.f);
+    if (q >= dtotal) return DnScales<DN_R>::zero();
     const int grp = g0 + (q / n_ent) * gstep;
     int inter;
     const float* sc;
     gemv_record(P, s_exp[q % n_ent], &inter, &sc);
-    return __ldg(reinterpret_cast<const float2*>(sc + 2 * inter + grp * DN_R));
+    return __ldg(reinterpret_cast<const typename DnScales<DN_R>::V*>(sc + 2 * inter + grp * DN_R));
   };
   // the first experts' rows stream in while the gate/up kernel finishes
   if (lane == 0)
     for (int q = 0; q < nslot && q < dtotal; ++q) issue(q);
-  float2 scq[DN_SCQ];
+  typename DnScales<DN_R>::V scq[DN_SCQ];
 #pragma unroll
   for (int i = 0; i < DN_SCQ; ++i) scq[i] = row_scales(i);
 
@@ -417,7 +429,8 @@ __global__ void __launch_bounds__(DN_MAX_NW * 32, 1) gemv_down_kernel(ExpertPara
       for (int t = 0; t < MT; ++t) yl[rr][t] = 0.f;
     for (int u = 0; u < n_ent; ++u) {
       const int q = r * n_ent + u, slot = q % nslot;
-      const float sd[DN_R] = {scq[0].x, scq[0].y};
+      float sd[DN_R];
+      DnScales<DN_R>::get(scq[0], sd);
 #pragma unroll
       for (int i = 0; i + 1 < DN_SCQ; ++i) scq[i] = scq[i + 1];
       scq[DN_SCQ - 1] = row_scales(q + DN_SCQ);
@@ -430,7 +443,9 @@ __global__ void __launch_bounds__(DN_MAX_NW * 32, 1) gemv_down_kernel(ExpertPara
       for (int p = s_off[u]; p < s_off[u] + s_cnt[u]; ++p) {
         const int t = s_tok[p];
         const float wgt = s_w[p];
-        float acc[DN_R] = {0.f, 0.f};
+        float acc[DN_R];
+#pragma unroll
+        for (int rr = 0; rr < DN_R; ++rr) acc[rr] = 0.f;
         for (int cc = lane; cc < nbI; cc += 32) {
           const uint4* a = reinterpret_cast<const uint4*>(s_qh + (size_t)p * im + (size_t)cc * QB);
           const uint4 a0 = a[0], a1 = a[1];
