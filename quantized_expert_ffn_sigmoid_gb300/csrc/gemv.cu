@@ -174,6 +174,10 @@ __global__ void __launch_bounds__(GU_THREADS, 1) gemv_gu_kernel(ExpertParams P) 
     int tok[NT];
 #pragma unroll
     for (int t = 0; t < NT; ++t) tok[t] = t < ntok ? s_pt[d.pair0 + t] : 0;
+    static_assert(GU_RPW == 2 && GU_SLOTS == 2, "row pair i of an item is in slot i");
+    float red[GU_RPW][2][NT];  // NT > 1: both row pairs' partials, reduced once per item
+    float rsg[GU_RPW], rsu[GU_RPW];  // their row scales (valid in lane 0)
+#pragma unroll
     for (int i = 0; i < GU_RPW; ++i) {
       const int seq = j * GU_RPW + i, slot = seq % GU_SLOTS;
       mbar_wait(&bars[warp * GU_SLOTS + slot], (uint32_t)(seq / GU_SLOTS) & 1u, status);
@@ -232,17 +236,57 @@ __global__ void __launch_bounds__(GU_THREADS, 1) gemv_gu_kernel(ExpertParams P) 
       const float sg = slot == 0 ? scg0 : scg1, su = slot == 0 ? scu0 : scu1;
       __syncwarp();
       if (lane == 0 && seq + GU_SLOTS < total) issue(seq + GU_SLOTS);
-#pragma unroll
-      for (int t = 0; t < NT; ++t) {
-        if (t < ntok) {
-          const float gs = warp_sum(pg[t]);
-          const float us = warp_sum(pu[t]);
-          if (lane == 0) {
-            const float gv = __fmul_rn(sg, gs);
-            const float uv = __fmul_rn(su, us);
-            hbuf[rp * TG + t] = __fmul_rn(__fdiv_rn(gv, 1.0f + expf(-gv)), uv);
-          }
+      if constexpr (NT == 1) {
+        const float gs = warp_sum(pg[0]);
+        const float us = warp_sum(pu[0]);
+        if (lane == 0) {
+          const float gv = __fmul_rn(sg, gs);
+          const float uv = __fmul_rn(su, us);
+          hbuf[rp * TG] = __fmul_rn(__fdiv_rn(gv, 1.0f + expf(-gv)), uv);
         }
+      } else {
+#pragma unroll
+        for (int t = 0; t < NT; ++t) {
+          red[i][0][t] = pg[t];
+          red[i][1][t] = pu[t];
+        }
+        rsg[i] = sg;
+        rsu[i] = su;
+      }
+    }
+    if constexpr (NT > 1) {
+      // The item's 4*NT sums (row pair, gate/up, position) over the warp's
+      // lanes by halving exchanges: lane pair 2v, 2v+1 ends with sum v; the
+      // up sum of (row pair, position) sits 2*NT lanes above the gate sum.
+      constexpr int NV = 4 * NT;
+      static_assert(NV == 16, "the exchange below is written for 16 sums");
+      float v[NV];
+#pragma unroll
+      for (int i = 0; i < GU_RPW; ++i)
+#pragma unroll
+        for (int gu = 0; gu < 2; ++gu)
+#pragma unroll
+          for (int t = 0; t < NT; ++t) v[(i * 2 + gu) * NT + t] = red[i][gu][t];
+#pragma unroll
+      for (int half = NV / 2, off = 16; half >= 1; half >>= 1, off >>= 1) {
+        const bool hi = (lane & off) != 0;
+#pragma unroll
+        for (int q = 0; q < half; ++q) {
+          const float send = hi ? v[q] : v[q + half];
+          const float keep = hi ? v[q + half] : v[q];
+          v[q] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+        }
+      }
+      v[0] += __shfl_xor_sync(0xffffffffu, v[0], 1);
+      const int vi = (lane >> 1) & (NV - 1);            // (row pair, gate/up, position)
+      const float us = __shfl_down_sync(0xffffffffu, v[0], 2 * NT);
+      const int i = vi / (2 * NT), t = vi % NT;
+      const float sg0 = __shfl_sync(0xffffffffu, rsg[0], 0), sg1 = __shfl_sync(0xffffffffu, rsg[1], 0);
+      const float su0 = __shfl_sync(0xffffffffu, rsu[0], 0), su1 = __shfl_sync(0xffffffffu, rsu[1], 0);
+      if ((lane & 1) == 0 && (vi / NT) % 2 == 0 && t < ntok) {
+        const float gv = __fmul_rn(i == 0 ? sg0 : sg1, v[0]);
+        const float uv = __fmul_rn(i == 0 ? su0 : su1, us);
+        hbuf[(warp + GU_NW * i) * TG + t] = __fmul_rn(__fdiv_rn(gv, 1.0f + expf(-gv)), uv);
       }
     }
     // one barrier per item: the tile's 32 h values are one Q8_0 block per
