@@ -20,6 +20,7 @@
 //   routing-weighted combine in registers, so no per-expert output buffer,
 //   counter or atomic is needed.  The order of the sum is
 //   fixed (entries in table order), so results are deterministic.
+#include <type_traits>
 #include "colimoe_internal.cuh"
 #include "gemv_common.cuh"
 
@@ -61,10 +62,8 @@ __global__ void __launch_bounds__(GU_THREADS, 1) gemv_gu_kernel(ExpertParams P) 
   off += (size_t)T * nb * 16;
   uint4* s_q1 = reinterpret_cast<uint4*>(sm_gu + off);                    // [T][nb] second halves
   off += (size_t)T * nb * 16;
-  float* s_d = reinterpret_cast<float*>(sm_gu + off);                     // [T][nb]
-  off += (size_t)T * nb * 4;
-  int* s_x = reinterpret_cast<int*>(sm_gu + off);                         // [T][nb]
-  off += (size_t)T * nb * 4;
+  float2* s_dc = reinterpret_cast<float2*>(sm_gu + off);                 // [T][nb] (scale, code-sum bits)
+  off += (size_t)T * nb * 8;
   float* s_h = reinterpret_cast<float*>(sm_gu + off);                     // [2][RA][TG]
   off += 2 * RA * TG * 4;
   int* s_pt = reinterpret_cast<int*>(sm_gu + off);                        // [P] pair -> position
@@ -104,8 +103,8 @@ __global__ void __launch_bounds__(GU_THREADS, 1) gemv_gu_kernel(ExpertParams P) 
     const int32_t* ptg = reinterpret_cast<const int32_t*>(ws + L.pair_token);
     for (int i = tid; i < hdr[H_NPAIRS]; i += GU_THREADS) s_pt[i] = ptg[i];
     for (int i = tid; i < T * nb; i += GU_THREADS) {
-      s_d[i] = __ldg(reinterpret_cast<const float*>(ws + L.dx) + i);
-      s_x[i] = __ldg(reinterpret_cast<const int32_t*>(ws + L.xs) + i);
+      s_dc[i] = make_float2(__ldg(reinterpret_cast<const float*>(ws + L.dx) + i),
+                            __int_as_float(__ldg(reinterpret_cast<const int32_t*>(ws + L.xs) + i)));
     }
   }
   __syncthreads();
@@ -116,7 +115,7 @@ __global__ void __launch_bounds__(GU_THREADS, 1) gemv_gu_kernel(ExpertParams P) 
 #pragma unroll
     for (int m = 0; m < RCPL; ++m) {
       const int cc = lane + 32 * m;
-      if (cc < nb) { ra0[m] = s_q0[cc]; ra1[m] = s_q1[cc]; rx[m] = s_x[cc]; rd[m] = s_d[cc]; }
+      if (cc < nb) { ra0[m] = s_q0[cc]; ra1[m] = s_q1[cc]; rx[m] = __float_as_int(s_dc[cc].y); rd[m] = s_dc[cc].x; }
     }
   }
   const uint64_t pol = policy_evict_first();
@@ -209,21 +208,22 @@ __global__ void __launch_bounds__(GU_THREADS, 1) gemv_gu_kernel(ExpertParams P) 
           }
         }
       } else {
+        // exactly ntok positions, unrolled: no per-position branches
+        auto blocks = [&](auto n_c) {
+          constexpr int N = decltype(n_c)::value;
 #pragma unroll 2
-        for (int cc = lane; cc < nb; cc += 32) {
-          WBlk<BITS> wg, wu;
-          wg.lds(grow + (size_t)cc * CBYTES);
-          wu.lds(urow + (size_t)cc * CBYTES);
+          for (int cc = lane; cc < nb; cc += 32) {
+            WBlk<BITS> wg, wu;
+            wg.lds(grow + (size_t)cc * CBYTES);
+            wu.lds(urow + (size_t)cc * CBYTES);
 #pragma unroll
-          for (int t = 0; t < NT; ++t) {
-            if (t < ntok) {
+            for (int t = 0; t < N; ++t) {
               const uint4 a0 = s_q0[tok[t] * nb + cc], a1 = s_q1[tok[t] * nb + cc];
-              const int corr = s_x[tok[t] * nb + cc];
-              const float dv = s_d[tok[t] * nb + cc];
-              const int ig = wg.dot(a0, a1, corr);
-              const int iu = wu.dot(a0, a1, corr);
-              pg[t] = fmaf(dv, (float)ig, pg[t]);
-              pu[t] = fmaf(dv, (float)iu, pu[t]);
+              const float2 dc = s_dc[tok[t] * nb + cc];
+              const int ig = wg.dot(a0, a1, __float_as_int(dc.y));
+              const int iu = wu.dot(a0, a1, __float_as_int(dc.y));
+              pg[t] = fmaf(dc.x, (float)ig, pg[t]);
+              pu[t] = fmaf(dc.x, (float)iu, pu[t]);
               if (DUMP && P.dump_gu) {
                 const size_t pb = (size_t)(d.pair0 + t) * 2 * L.imax;
                 P.dump_gu[(pb + row) * nb + cc] = ig;
@@ -231,6 +231,12 @@ __global__ void __launch_bounds__(GU_THREADS, 1) gemv_gu_kernel(ExpertParams P) 
               }
             }
           }
+        };
+        switch (ntok) {
+          case 1: blocks(std::integral_constant<int, 1>{}); break;
+          case 2: blocks(std::integral_constant<int, NT >= 2 ? 2 : 1>{}); break;
+          case 3: blocks(std::integral_constant<int, NT >= 3 ? 3 : 1>{}); break;
+          default: blocks(std::integral_constant<int, NT>{}); break;
         }
       }
       const float sg = slot == 0 ? scg0 : scg1, su = slot == 0 ? scu0 : scu1;
