@@ -107,6 +107,17 @@ __device__ __forceinline__ void tmem_ld16_nowait(uint32_t taddr, uint32_t* r) {
 }
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
+// (a0, a1) = (d0 * v0 + a0, d1 * v1 + a1), each rounded once: one paired fp32 FMA
+__device__ __forceinline__ void ffma2(float& a0, float& a1, float d0, float d1, float v0, float v1) {
+  asm("{\n\t.reg .b64 ra, rb, rc;\n\t"
+      "mov.b64 ra, {%2, %3};\n\t"
+      "mov.b64 rb, {%4, %5};\n\t"
+      "mov.b64 rc, {%0, %1};\n\t"
+      "fma.rn.f32x2 rc, ra, rb, rc;\n\t"
+      "mov.b64 {%0, %1}, rc;\n\t}"
+      : "+f"(a0), "+f"(a1) : "f"(d0), "f"(d1), "f"(v0), "f"(v1));
+}
+
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
   uint32_t d;
   asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
@@ -477,10 +488,10 @@ __global__ void __launch_bounds__(PF_THREADS2, 1) pf_gemm(const __grid_constant_
 #pragma unroll
               for (int j4 = 0; j4 < PF_EPC / 4; ++j4) {
                 const float4 d = d4[j4];
-                acc[m][4 * j4] = fmaf(d.x, __uint_as_float(v[i][4 * j4]), acc[m][4 * j4]);
-                acc[m][4 * j4 + 1] = fmaf(d.y, __uint_as_float(v[i][4 * j4 + 1]), acc[m][4 * j4 + 1]);
-                acc[m][4 * j4 + 2] = fmaf(d.z, __uint_as_float(v[i][4 * j4 + 2]), acc[m][4 * j4 + 2]);
-                acc[m][4 * j4 + 3] = fmaf(d.w, __uint_as_float(v[i][4 * j4 + 3]), acc[m][4 * j4 + 3]);
+                ffma2(acc[m][4 * j4], acc[m][4 * j4 + 1], d.x, d.y, __uint_as_float(v[i][4 * j4]),
+                      __uint_as_float(v[i][4 * j4 + 1]));
+                ffma2(acc[m][4 * j4 + 2], acc[m][4 * j4 + 3], d.z, d.w, __uint_as_float(v[i][4 * j4 + 2]),
+                      __uint_as_float(v[i][4 * j4 + 3]));
               }
               if (DUMP) {
                 const int row = it.mt * PF_M + rr, bq2 = ch * PF_CB + blk;
