@@ -196,13 +196,14 @@ decode_layer_kernel(ExpertParams P, const float* __restrict__ x, const int32_t* 
   float4 rwv[DK_RWL];
   float bias_reg = 0.f;
   if (MODE == DM_ROUTE) {
-    if (lane == 0) top_up(0, my_sh * DK_RPW);
+    // the router's weights first: the logits of every CTA gate the routing
     if (r_task) {
 #pragma unroll
       for (int m = 0; m < DK_RWL; ++m)
         if (lane + 32 * m < rn4) rwv[m] = __ldg(r_w4 + lane + 32 * m);
     }
     if (tid < E) bias_reg = __ldg(R.bias + tid);
+    if (lane == 0) top_up(0, my_sh * DK_RPW);
   }
   pdl_wait();
   pdl_launch_dependents();
