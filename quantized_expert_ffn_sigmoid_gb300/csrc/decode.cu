@@ -20,8 +20,8 @@
 //             the CTA-wide selection itself (identical in every CTA), so no
 //             grid barrier and no separate router launch are needed.  The shared
 //             expert's gate/up tiles come first in the work order: their rows
-//             are requested before the grid dependency wait and computed
-//             before the routing is known.
+//             are requested as soon as the CTA's logits are published and
+//             computed before the routing is known.
 // Phases:
 //   1. gate/up: the 32-row tiles of every selected expert (shared first) are
 //      dealt round-robin to the CTAs; each warp streams its row pairs with
@@ -196,14 +196,15 @@ decode_layer_kernel(ExpertParams P, const float* __restrict__ x, const int32_t* 
   float4 rwv[DK_RWL];
   float bias_reg = 0.f;
   if (MODE == DM_ROUTE) {
-    // the router's weights first: the logits of every CTA gate the routing
+    // only the router's weights before the wait: the logits of every CTA
+    // gate the routing (the shared tiles are requested once this CTA's
+    // logits are out)
     if (r_task) {
 #pragma unroll
       for (int m = 0; m < DK_RWL; ++m)
         if (lane + 32 * m < rn4) rwv[m] = __ldg(r_w4 + lane + 32 * m);
     }
     if (tid < E) bias_reg = __ldg(R.bias + tid);
-    if (lane == 0) top_up(0, my_sh * DK_RPW);
   }
   pdl_wait();
   pdl_launch_dependents();
@@ -237,6 +238,7 @@ decode_layer_kernel(ExpertParams P, const float* __restrict__ x, const int32_t* 
       for (int s = 0; s < rsplits; ++s) l += s_rpart[tid * rsplits + s];
       st_relaxed_u64(rwords + e, ((uint64_t)(s_epoch + 1u) << 32) | __float_as_uint(l));
     }
+    if (lane == 0) top_up(0, my_sh * DK_RPW);  // the shared tiles of this CTA
   }
 
   // ---------------------------------------------------------- Q8_0 of x
