@@ -18,10 +18,11 @@
 //             in order in shared memory) and publishes each as one 64-bit
 //             word (value, call tag); every CTA polls the E words, then runs
 //             the CTA-wide selection itself (identical in every CTA), so no
-//             grid barrier and no separate router launch are needed.  The shared
-//             expert's gate/up tiles come first in the work order: their rows
-//             are requested as soon as the CTA's logits are published and
-//             computed before the routing is known.
+//             grid barrier and no separate router launch are needed.  Only
+//             the router's weights are read before the logits are out; the
+//             shared expert's tiles (the first items of the first CTAs) are
+//             then prefetched into L2 only, so that no shared-memory slot waits
+//             on them while the routing completes.
 // Phases:
 //   1. gate/up: the 32-row tiles of every selected expert (shared first) are
 //      dealt round-robin to the CTAs; each warp streams its row pairs with
@@ -43,6 +44,11 @@
 #include "select_cta.cuh"
 
 namespace colimoe {
+
+// bytes (16-byte aligned, a multiple of 16) into L2, no destination
+__device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
 
 constexpr int DK_THREADS = 512;
 constexpr int DK_NW = DK_THREADS / 32;       // 16 warps
@@ -186,7 +192,6 @@ decode_layer_kernel(ExpertParams P, const float* __restrict__ x, const int32_t* 
   __syncthreads();
 
   // ---------------------------------------------------------- before the dependency wait: weights only
-  const int my_sh = n_sh_items > (int)blockIdx.x ? (n_sh_items - 1 - (int)blockIdx.x) / G + 1 : 0;
   // router task of this warp: expert blockIdx.x * epc + warp / splits, K split warp % splits
   const int rsplits = MODE == DM_ROUTE ? R.splits : 1;
   const int rn4 = H / 4 / rsplits;
@@ -197,8 +202,7 @@ decode_layer_kernel(ExpertParams P, const float* __restrict__ x, const int32_t* 
   float bias_reg = 0.f;
   if (MODE == DM_ROUTE) {
     // only the router's weights before the wait: the logits of every CTA
-    // gate the routing (the shared tiles are requested once this CTA's
-    // logits are out)
+    // gate the routing
     if (r_task) {
 #pragma unroll
       for (int m = 0; m < DK_RWL; ++m)
@@ -238,7 +242,18 @@ decode_layer_kernel(ExpertParams P, const float* __restrict__ x, const int32_t* 
       for (int s = 0; s < rsplits; ++s) l += s_rpart[tid * rsplits + s];
       st_relaxed_u64(rwords + e, ((uint64_t)(s_epoch + 1u) << 32) | __float_as_uint(l));
     }
-    if (lane == 0) top_up(0, my_sh * DK_RPW);  // the shared tiles of this CTA
+    // this CTA's shared tile (its first item) into L2 while the routing
+    // completes: no shared-memory slot is held, so the routed tiles' copies
+    // are not held up behind it (each warp: two consecutive gate and up rows)
+    if ((int)blockIdx.x < n_sh_items && lane == 0) {
+      const int it = blockIdx.x;
+      int inter;
+      const float* sc;
+      const uint8_t* rec = gemv_record(P, E + it / tps, &inter, &sc);
+      const int row = (it % tps) * RA + warp * DK_RPW;
+      prefetch_l2(rec + (size_t)row * rb, (uint32_t)(DK_RPW * rb));
+      prefetch_l2(rec + (size_t)(inter + row) * rb, (uint32_t)(DK_RPW * rb));
+    }
   }
 
   // ---------------------------------------------------------- Q8_0 of x
@@ -382,14 +397,7 @@ decode_layer_kernel(ExpertParams P, const float* __restrict__ x, const int32_t* 
   };
 
   // ---------------------------------------------------------- routing
-  int j0 = 0;
   if (MODE == DM_ROUTE) {
-    // a shared tile dealt to this CTA first needs no routing: compute it now
-    // (its requantisation waits for the pair numbering)
-    if (my_sh > 0) {
-      gu_item(0, my_sh * DK_RPW);
-      j0 = 1;
-    }
     // every expert's logit word, once it carries this call's tag (bounded wait)
     float* s_logit = reinterpret_cast<float*>(dact);
     const uint32_t tag = s_epoch + 1u;
@@ -560,9 +568,8 @@ decode_layer_kernel(ExpertParams P, const float* __restrict__ x, const int32_t* 
   // ---------------------------------------------------------- phase 1: gate / up
   const int nmine = nA > (int)blockIdx.x ? (nA - 1 - (int)blockIdx.x) / G + 1 : 0;
   const int total = nmine * DK_RPW;
-  if (lane == 0) top_up(j0 * DK_RPW, total);
-  if (j0 > 0) requant_item(0);
-  for (int j = j0; j < nmine; ++j) {
+  if (lane == 0) top_up(0, total);
+  for (int j = 0; j < nmine; ++j) {
     gu_item(j, total);
     requant_item(j);
   }
