@@ -4,7 +4,9 @@ TEST INFRASTRUCTURE ONLY (see the package docstring).
 
 Source: colibrì v1.0 README, "What's implemented" (integer-dot kernels on
 Q8_0-style int8 activations; int8 / packed int4 weights with per-row scales)
-and "Experimental Metal backend" (the routed-expert SwiGLU).
+and "Experimental Metal backend" (the routed-expert SwiGLU).  Group-scaled
+int4 ("gs64": one scale per 64 weights of a row instead of one per row) is the
+container the colibri GLM-5.2 quick start recommends ("2. Get the model").
 
 Per expert with intermediate size I, weights gate [I,H], up [I,H], down [H,I]
 (codes ``q``, per-row fp32 scales ``s``); per token with Q8_0 codes ``qx`` and
@@ -15,6 +17,11 @@ block scales ``dx``:
 * ``h = silu(g) * u`` with ``silu(g) = g / (1 + exp(-g))``;
 * ``h`` is re-quantised to Q8_0 (every product takes int8 activations);
 * ``o[c] = s_d[c] * sum_b dh[b] * acc_d[c,b]``.
+
+With group scales (``group`` = 64, two Q8_0 blocks per group) the row scale
+moves inside the block sum: ``g[r] = sum_b s_g[r, b // 2] * dx[b] * acc_g[r,b]``
+(reading: the pages give the format, not the order of the scalings; this
+is the plain definition, the dot product of the dequantised operands).
 
 fp64 throughout except the Q8_0 step, which takes ``float32(h)`` and decides
 the codes in fp32 (see ``quant.py``).
@@ -50,15 +57,30 @@ def block_dots(wq: np.ndarray, qx: np.ndarray) -> np.ndarray:
 def _scaled_rows(acc, d, s):
     """fp64 ``s[r] * sum_b d[t,b] * acc[t,r,b]`` and its fp32-evaluation bound.
 
+    ``s`` [R] row scales, or [R, nb/bpg] group scales (one per ``bpg``
+    consecutive blocks), then ``sum_b s[r, b // bpg] * d[t,b] * acc[t,r,b]``.
     The bound is the standard worst case for evaluating the same sum in fp32
-    in any order: (terms + 4) * u * s * sum |d * acc| (Higham, gamma_n)."""
+    in any order: (terms + 4) * u * sum |s * d * acc| (Higham, gamma_n)."""
     d64 = np.asarray(d, np.float64)[:, None, :]
     terms = d64 * acc.astype(np.float64)
-    val = np.asarray(s, np.float64)[None, :] * terms.sum(axis=2)
+    s64 = np.asarray(s, np.float64)
     nterm = acc.shape[2]
-    bound = (nterm + 4) * U32 * np.abs(np.asarray(s, np.float64))[None, :] * \
-        np.abs(terms).sum(axis=2)
+    if s64.ndim == 2:
+        bpg = nterm // s64.shape[1]
+        terms = terms * np.repeat(s64, bpg, axis=1)[None, :, :]
+        return terms.sum(axis=2), (nterm + 4) * U32 * np.abs(terms).sum(axis=2)
+    val = s64[None, :] * terms.sum(axis=2)
+    bound = (nterm + 4) * U32 * np.abs(s64)[None, :] * np.abs(terms).sum(axis=2)
     return val, bound
+
+
+def _split_scales(scales, H: int, I: int, group: int):
+    """(s_g, s_u, s_d): per-row [I], [I], [H], or per group [I, H/g], [I, H/g], [H, I/g]."""
+    if not group:
+        return scales[:I], scales[I:2 * I], scales[2 * I:2 * I + H]
+    n = I * H // group
+    return (scales[:n].reshape(I, H // group), scales[n:2 * n].reshape(I, H // group),
+            scales[2 * n:3 * n].reshape(H, I // group))
 
 
 def _split_record(record: np.ndarray, H: int, I: int, bits: int):
@@ -74,8 +96,9 @@ def _split_record(record: np.ndarray, H: int, I: int, bits: int):
     return wg, wu, wd
 
 
-def expert_ffn(record, scales, H: int, I: int, bits: int, qx, dx):
+def expert_ffn(record, scales, H: int, I: int, bits: int, qx, dx, group: int = 0):
     """Run one expert on tokens with Q8_0 activations ``qx`` [T,H], ``dx``.
+    ``group``: 0 for per-row scales, else the weights per group scale (64).
 
     Returns a dict with the integer accumulators (``acc_g``, ``acc_u``,
     ``acc_d``), ``g``, ``u``, ``h`` (fp64), the requantised ``qh``/``dh``,
@@ -85,7 +108,7 @@ def expert_ffn(record, scales, H: int, I: int, bits: int, qx, dx):
     qx = np.atleast_2d(qx)
     dx = np.atleast_2d(dx)
     scales = np.asarray(scales, np.float32)
-    s_g, s_u, s_d = scales[:I], scales[I:2 * I], scales[2 * I:2 * I + H]
+    s_g, s_u, s_d = _split_scales(scales, H, I, group)
     wg, wu, wd = _split_record(record, H, I, bits)
     acc_g = block_dots(wg, qx)
     acc_u = block_dots(wu, qx)
@@ -107,7 +130,7 @@ def expert_ffn(record, scales, H: int, I: int, bits: int, qx, dx):
                 h_err=eh, qh=qh, dh=dh, qh_stable=stable, o=o, o_err=eo)
 
 
-def expert_ffn_dequant_fp64(record, scales, H: int, I: int, bits: int, x):
+def expert_ffn_dequant_fp64(record, scales, H: int, I: int, bits: int, x, group: int = 0):
     """The same expert evaluated by plain fp64 matrix products on dequantised
     operands: W = s * q for the weights, x and h as Q8_0 round trips.
 
@@ -115,11 +138,12 @@ def expert_ffn_dequant_fp64(record, scales, H: int, I: int, bits: int, x):
     regroups the sum), so the two agree to fp64 rounding; used as a pin."""
     from .quant import q8_0_dequantize
     scales = np.asarray(scales, np.float64)
-    s_g, s_u, s_d = scales[:I], scales[I:2 * I], scales[2 * I:2 * I + H]
+    s_g, s_u, s_d = _split_scales(scales, H, I, group)
     wg, wu, wd = _split_record(record, H, I, bits)
-    Wg = wg.astype(np.float64) * s_g[:, None]
-    Wu = wu.astype(np.float64) * s_u[:, None]
-    Wd = wd.astype(np.float64) * s_d[:, None]
+
+    def deq(w, s):  # W = s * q, the scale of a row or of each group of a row
+        return w.astype(np.float64) * (np.repeat(s, group, axis=1) if group else s[:, None])
+    Wg, Wu, Wd = deq(wg, s_g), deq(wu, s_u), deq(wd, s_d)
     qx, dx = q8_0_quantize(np.atleast_2d(x).astype(np.float32))
     xs = q8_0_dequantize(qx, dx)
     g = xs @ Wg.T

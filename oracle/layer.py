@@ -86,7 +86,8 @@ def moe_forward(shape, get_record, x: np.ndarray, idx: np.ndarray, w: np.ndarray
         sel = np.argwhere(idx == e)              # (t, j) ascending
         toks = sel[:, 0]
         rec, sc = get_record("routed", int(e))
-        out = expert_ffn(rec, sc, H, shape.inter, shape.weight_bits, qx[toks], dx[toks])
+        out = expert_ffn(rec, sc, H, shape.inter, shape.weight_bits, qx[toks], dx[toks],
+                         getattr(shape, "group_size", 0))
         for n, (t, j) in enumerate(sel):
             y[t] += w[t, j] * out["o"][n]
             yerr[t] += abs(w[t, j]) * (out["o_err"][n] + np.abs(out["o"][n]) * 4 * U32)
@@ -96,7 +97,8 @@ def moe_forward(shape, get_record, x: np.ndarray, idx: np.ndarray, w: np.ndarray
             pairs[("routed", int(e))] = out
     for s in range(shape.n_shared):
         rec, sc = get_record("shared", s)
-        out = expert_ffn(rec, sc, H, shape.shared_inter, shape.weight_bits, qx, dx)
+        out = expert_ffn(rec, sc, H, shape.shared_inter, shape.weight_bits, qx, dx,
+                         getattr(shape, "group_size", 0))
         y += out["o"]
         yerr += out["o_err"]
         if keep_pairs:
@@ -126,9 +128,11 @@ def dense_reference(shape, get_record, x, gate_dense: np.ndarray):
     y = np.zeros((x.shape[0], H))
     for e in range(shape.n_experts):
         rec, sc = get_record("routed", e)
-        o = expert_ffn(rec, sc, H, shape.inter, shape.weight_bits, qx, dx)["o"]
+        o = expert_ffn(rec, sc, H, shape.inter, shape.weight_bits, qx, dx,
+                         getattr(shape, "group_size", 0))["o"]
         y += gate_dense[:, e:e + 1] * o
     for s in range(shape.n_shared):
         rec, sc = get_record("shared", s)
-        y += expert_ffn(rec, sc, H, shape.shared_inter, shape.weight_bits, qx, dx)["o"]
+        y += expert_ffn(rec, sc, H, shape.shared_inter, shape.weight_bits, qx, dx,
+                         getattr(shape, "group_size", 0))["o"]
     return y

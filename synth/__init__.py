@@ -163,6 +163,14 @@ def quantize_rows_int(z: np.ndarray, qmax: int):
     return q.astype(np.int8), amax[:, 0]
 
 
+def quantize_groups_int(z: np.ndarray, qmax: int, group: int):
+    """``quantize_rows_int`` applied to every run of ``group`` consecutive
+    elements of a row: codes [rows, K] and the group maxima [rows, K/group]."""
+    rows, k = z.shape
+    q, amax = quantize_rows_int(z.reshape(rows * (k // group), group), qmax)
+    return q.reshape(rows, k), amax.reshape(rows, k // group)
+
+
 def scale_from_amax(amax: np.ndarray, std: float, qmax: int) -> np.ndarray:
     c = std / (SIGMA_Z * qmax)
     return (amax.astype(np.float64) * c).astype(np.float32)
@@ -189,6 +197,7 @@ class LayerShape:
     shared_inter: int
     weight_bits: int
     routed_scaling_factor: float
+    group_size: int = 0   # 0: one scale per output row; 64: one per 64 weights of a row
 
     @property
     def qmax(self) -> int:
@@ -203,6 +212,8 @@ class LayerShape:
 
     def scale_count(self, inter: int | None = None) -> int:
         i = self.inter if inter is None else inter
+        if self.group_size:
+            return 3 * i * self.hidden // self.group_size
         return 2 * i + self.hidden
 
 
@@ -218,13 +229,18 @@ def expert_matrix_key(seed, layer, kind, expert, matrix):
 
 
 def expert_matrix(shape: LayerShape, seed, layer, kind, expert, matrix):
-    """Return (codes int8 [rows,K], packed bytes [rows, row_bytes], scales f32)."""
+    """Return (codes int8 [rows,K], packed bytes [rows, row_bytes], scales f32:
+    [rows], or [rows * K/group] row-major for group-scaled weights)."""
     inter = shape.inter if kind == "routed" else shape.shared_inter
     rows, k = ((inter, shape.hidden) if matrix < 2 else (shape.hidden, inter))
     key = expert_matrix_key(seed, layer, kind, expert, matrix)
     z = normal_int(key, rows * k).reshape(rows, k)
-    q, amax = quantize_rows_int(z, shape.qmax)
-    scales = scale_from_amax(amax, WEIGHT_STD, shape.qmax)
+    if shape.group_size:
+        q, amax = quantize_groups_int(z, shape.qmax, shape.group_size)
+        scales = scale_from_amax(amax, WEIGHT_STD, shape.qmax).reshape(-1)
+    else:
+        q, amax = quantize_rows_int(z, shape.qmax)
+        scales = scale_from_amax(amax, WEIGHT_STD, shape.qmax)
     packed = pack_int4_rows(q) if shape.weight_bits == 4 else q.view(np.uint8)
     return q, packed, scales
 
@@ -301,6 +317,13 @@ GLM = LayerShape(hidden=6144, n_experts=256, n_groups=8, topk_group=4, top_k=8,
 GLM_INT8 = LayerShape(hidden=6144, n_experts=256, n_groups=8, topk_group=4,
                       top_k=8, inter=2048, n_shared=1, shared_inter=2048,
                       weight_bits=8, routed_scaling_factor=2.5)
+# group-scaled int4 ("gs64": one scale per 64 weights of a row)
+TINY_GS64 = LayerShape(hidden=256, n_experts=16, n_groups=4, topk_group=2, top_k=4,
+                       inter=128, n_shared=1, shared_inter=128, weight_bits=4,
+                       routed_scaling_factor=2.5, group_size=64)
+GLM_GS64 = LayerShape(hidden=6144, n_experts=256, n_groups=8, topk_group=4, top_k=8,
+                      inter=2048, n_shared=1, shared_inter=2048, weight_bits=4,
+                      routed_scaling_factor=2.5, group_size=64)
 
 WORKLOADS = {
     # name: (shape, seed, positions per call, calls)

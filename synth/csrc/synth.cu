@@ -1,6 +1,7 @@
 // Device twin of the seeded input generator in synth/__init__.py:
 // Philox4x32-10 (Salmon et al., SC'11) keyed per tensor, Irwin-Hall sums of
-// four 16-bit uniforms, per-row absmax integer quantisation and int4 packing.
+// four 16-bit uniforms, per-row (or per-64-element) absmax integer
+// quantisation and int4 packing.
 // Every step is integer arithmetic except one IEEE double multiply and one
 // round-to-nearest conversion per scale, so it matches the numpy version bit
 // for bit.  Holds none of the MoE layer's arithmetic.
@@ -70,6 +71,33 @@ __global__ void __launch_bounds__(256) quant_rows_kernel(uint32_t k0, uint32_t k
   }
 }
 
+// One warp per run of 64 elements of a row (32 draws, one per lane): the run's
+// absmax, its codes and its scale (scales [rows][K/64], row-major).
+__global__ void __launch_bounds__(256) quant_groups64_kernel(uint32_t k0, uint32_t k1, int rows, int K, int qmax,
+                                                             double c, int bits, uint8_t* __restrict__ out,
+                                                             float* __restrict__ scales) {
+  const int half = K / 2, ng = K / 64, lane = threadIdx.x & 31;
+  const long long nw = (long long)rows * ng;
+  for (long long w = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5; w < nw;
+       w += ((long long)gridDim.x * blockDim.x) >> 5) {
+    const int row = (int)(w / ng), g = (int)(w % ng);
+    const int j = g * 32 + lane;  // draw index within the row
+    int z0, z1;
+    pair_normals((uint64_t)row * (uint64_t)half + j, k0, k1, &z0, &z1);
+    int m = max(abs(z0), abs(z1));
+#pragma unroll
+    for (int o = 16; o; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
+    const int q0 = quant(z0, m, qmax), q1 = quant(z1, m, qmax);
+    if (bits == 4) {
+      out[(size_t)row * half + j] = (uint8_t)((q0 + 8) | ((q1 + 8) << 4));
+    } else {
+      out[(size_t)row * K + 2 * j] = (uint8_t)(int8_t)q0;
+      out[(size_t)row * K + 2 * j + 1] = (uint8_t)(int8_t)q1;
+    }
+    if (lane == 0) scales[(size_t)row * ng + g] = __double2float_rn((double)m * c);
+  }
+}
+
 __global__ void normal_f32_kernel(uint32_t k0, uint32_t k1, long long n, float mul, float* __restrict__ out) {
   const long long pairs = (n + 1) / 2;
   for (long long j = (long long)blockIdx.x * blockDim.x + threadIdx.x; j < pairs;
@@ -91,6 +119,17 @@ int synth_quant_rows(uint32_t k0, uint32_t k1, int rows, int K, int qmax, double
   if (K % 2 || rows <= 0) return -1;
   int grid = rows < 4096 ? rows : 4096;
   quant_rows_kernel<<<grid, 256, 0, st>>>(k0, k1, rows, K, qmax, c, bits, static_cast<uint8_t*>(out), scales);
+  return cudaGetLastError() == cudaSuccess ? 0 : -2;
+}
+
+// The same with one scale per 64 elements of a row (K a multiple of 64).
+int synth_quant_groups64(uint32_t k0, uint32_t k1, int rows, int K, int qmax, double c, int bits, void* out,
+                         float* scales, cudaStream_t st) {
+  if (K % 64 || rows <= 0) return -1;
+  const long long warps = (long long)rows * (K / 64);
+  const long long blocks = (warps + 7) / 8 < 65536 ? (warps + 7) / 8 : 65536;
+  quant_groups64_kernel<<<(unsigned)blocks, 256, 0, st>>>(k0, k1, rows, K, qmax, c, bits, static_cast<uint8_t*>(out),
+                                                          scales);
   return cudaGetLastError() == cudaSuccess ? 0 : -2;
 }
 

@@ -25,6 +25,7 @@ def _lib():
         lib.synth_quant_rows.argtypes = [ctypes.c_uint32, ctypes.c_uint32, ctypes.c_int, ctypes.c_int,
                                          ctypes.c_int, ctypes.c_double, ctypes.c_int, ctypes.c_void_p,
                                          ctypes.c_void_p, ctypes.c_void_p]
+        lib.synth_quant_groups64.argtypes = lib.synth_quant_rows.argtypes
         lib.synth_normal_f32.argtypes = [ctypes.c_uint32, ctypes.c_uint32, ctypes.c_longlong,
                                          ctypes.c_float, ctypes.c_void_p, ctypes.c_void_p]
         _LIB = lib
@@ -47,8 +48,13 @@ def fill_expert_records(shape: LayerShape, seed, layer, kind, experts, out: torc
     rbH = shape.row_bytes(H)
     rbI = shape.row_bytes(inter)
     offs = [0, inter * rbH, 2 * inter * rbH]
-    soffs = [0, inter, 2 * inter]
     dims = [(inter, H), (inter, H), (H, inter)]
+    gs = shape.group_size
+    if gs not in (0, 64):
+        raise ValueError("the device generator draws per-row or 64-element groups")
+    per = [r if not gs else r * k // gs for r, k in dims]
+    soffs = [0, per[0], per[0] + per[1]]
+    fn = lib.synth_quant_groups64 if gs else lib.synth_quant_rows
     for n, e in enumerate(experts):
         row = first_slot + n
         base = out[row].data_ptr()
@@ -56,7 +62,7 @@ def fill_expert_records(shape: LayerShape, seed, layer, kind, experts, out: torc
         for m in range(3):
             k0, k1 = expert_matrix_key(seed, layer, kind, int(e), m)
             rows, K = dims[m]
-            rc = lib.synth_quant_rows(k0, k1, rows, K, qmax, c, shape.weight_bits,
+            rc = fn(k0, k1, rows, K, qmax, c, shape.weight_bits,
                                       ctypes.c_void_p(base + offs[m]),
                                       ctypes.c_void_p(sbase + 4 * soffs[m]), _stream())
             if rc:
