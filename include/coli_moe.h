@@ -78,6 +78,8 @@ typedef struct coli_moe_cfg {
     int32_t shared_inter;           /* intermediate size of shared experts  */
     int32_t weight_bits;            /* 4: packed int4, 8: int8              */
     float   routed_scaling_factor;  /* multiplies the renormalised weights  */
+    int32_t group_size;             /* 0: one scale per output row;
+                                       64: one per 64 weights of a row ("gs64") */
 } coli_moe_cfg;
 
 /* Expert weights.  One expert "record" is its three matrices stored adjacent
@@ -93,7 +95,12 @@ typedef struct coli_moe_cfg {
  * record_bytes = (2*Ie*H + H*Ie) * weight_bits / 8.
  * Scales are fp32 per output row, consecutive per expert:
  *     expert_scales[e * (2*I + H) + {0..I-1: gate, I..2I-1: up, 2I..: down}]
- * and likewise shared_scales with shared_inter. */
+ * and likewise shared_scales with shared_inter.
+ * With group_size 64 (the group-scaled container the colibri GLM-5.2 quick
+ * start recommends, "2. Get the model") every run of 64 weights of a row has
+ * its own fp32 scale: per expert 3*I*H/64 scales,
+ *     gate [I][H/64] | up [I][H/64] | down [H][I/64], each row-major,
+ * and an output is sum over Q8_0 blocks b of s[row][b/2] * d_b * (block dot). */
 typedef struct coli_moe_weights {
     const void*  experts;        /* [n_experts] records                 */
     const float* expert_scales;  /* [n_experts][2*inter + hidden]       */

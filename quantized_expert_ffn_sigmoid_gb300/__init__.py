@@ -39,12 +39,14 @@ class Cfg(ctypes.Structure):
                 ("n_groups", ctypes.c_int32), ("topk_group", ctypes.c_int32),
                 ("top_k", ctypes.c_int32), ("inter", ctypes.c_int32),
                 ("n_shared", ctypes.c_int32), ("shared_inter", ctypes.c_int32),
-                ("weight_bits", ctypes.c_int32), ("routed_scaling_factor", ctypes.c_float)]
+                ("weight_bits", ctypes.c_int32), ("routed_scaling_factor", ctypes.c_float),
+                ("group_size", ctypes.c_int32)]
 
     @classmethod
     def of(cls, shape) -> "Cfg":
-        """From any object with the same field names (e.g. synth.LayerShape)."""
-        return cls(*(getattr(shape, f) for f, _ in cls._fields_))
+        """From any object with the same field names (e.g. synth.LayerShape);
+        a missing group_size means per-row scales."""
+        return cls(*(getattr(shape, f, 0) if f == "group_size" else getattr(shape, f) for f, _ in cls._fields_))
 
 
 class Weights(ctypes.Structure):

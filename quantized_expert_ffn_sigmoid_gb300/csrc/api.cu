@@ -46,6 +46,7 @@ int check_cfg(const coli_moe_cfg* c) {
   if (c->n_shared < 0 || c->n_shared > MAX_SHARED) return COLI_EINVAL;
   if (c->n_shared > 0 && (c->shared_inter <= 0 || c->shared_inter % 128)) return COLI_EINVAL;
   if (c->weight_bits != 4 && c->weight_bits != 8) return COLI_EINVAL;
+  if (c->group_size != 0 && c->group_size != 64) return COLI_EINVAL;
   if (!(c->routed_scaling_factor == c->routed_scaling_factor)) return COLI_EINVAL;
   // a gate+up stage must hold at least one row pair, a down stage four rows
   if (2 * row_bytes(c->hidden, c->weight_bits) > SB) return COLI_EUNSUPPORTED;
@@ -54,6 +55,10 @@ int check_cfg(const coli_moe_cfg* c) {
   if (c->hidden % RB) return COLI_EUNSUPPORTED;
   return COLI_OK;
 }
+
+// The fast paths take per-row scales; group-scaled weights run on the
+// general expert kernel.
+bool per_row(const coli_moe_cfg& c) { return c.group_size == 0; }
 
 coli_moe_cfg normalized(const coli_moe_cfg* c) {
   coli_moe_cfg n = *c;
@@ -121,24 +126,24 @@ int do_experts(const coli_moe_cfg& c, const coli_moe_weights* w, int T, const fl
                uint8_t* ws, const Layout& L, cudaStream_t st, int32_t* dump_gu, int32_t* dump_d,
                const float* x = nullptr, const int32_t* idx = nullptr) {
   const ExpertParams P = expert_params(c, w, topk_w, y, ws, L, dump_gu, dump_d);
-  if (T == 1 && decode_fits(c)) {
+  if (T == 1 && per_row(c) && decode_fits(c)) {
     const int n_sm = sm_count();
     if (n_sm <= 0) return COLI_ECUDA;
     return rc_of(launch_decode(P, x, idx, x == nullptr, n_sm, st, dump_gu || dump_d));
   }
-  if (prefill_fits(c, T)) {
+  if (per_row(c) && prefill_fits(c, T)) {
     // many positions: the expert products on the tensor cores
     const int n_sm = sm_count();
     if (n_sm <= 0) return COLI_ECUDA;
     return rc_of(launch_prefill(P, T, n_sm, st, dump_gu || dump_d));
   }
-  if (T <= GEMV_MAX_T && gemv_fits(c, L)) {
+  if (T <= GEMV_MAX_T && per_row(c) && gemv_fits(c, L)) {
     // a few positions: stream the weights through the two GEMV kernels
     const int n_sm = sm_count();
     if (n_sm <= 0) return COLI_ECUDA;
     return rc_of(launch_gemv(P, n_sm, st, dump_gu || dump_d));
   }
-  if (sb_fits(c, L)) {
+  if (per_row(c) && sb_fits(c, L)) {
     // up to a few dozen positions: weight rows on lanes, K split over warps
     const int n_sm = sm_count();
     if (n_sm <= 0) return COLI_ECUDA;
@@ -255,7 +260,7 @@ int coli_moe_forward(const coli_moe_cfg* cfg, const coli_moe_weights* weights, c
   Layout L;
   if ((rc = check_ws(c, T, ws, ws_bytes, &L))) return rc;
   uint8_t* w8 = static_cast<uint8_t*>(ws);
-  if (T == 1 && decode_fits(c)) return do_experts(c, weights, T, topk_w, y, w8, L, stream, nullptr, nullptr, x, topk_idx);
+  if (T == 1 && per_row(c) && decode_fits(c)) return do_experts(c, weights, T, topk_w, y, w8, L, stream, nullptr, nullptr, x, topk_idx);
   if ((rc = do_dispatch(c, x, T, topk_idx, w8, L, stream))) return rc;
   return do_experts(c, weights, T, topk_w, y, w8, L, stream, nullptr, nullptr);
 }
@@ -276,7 +281,7 @@ int coli_moe_layer(const coli_moe_cfg* cfg, const coli_moe_weights* weights, con
   Layout L;
   if ((rc = check_ws(c, T, ws, ws_bytes, &L))) return rc;
   uint8_t* w8 = static_cast<uint8_t*>(ws);
-  if (T == 1 && decode_route_fits(c)) {
+  if (T == 1 && per_row(c) && decode_route_fits(c)) {
     const int n_sm = sm_count();
     if (n_sm <= 0) return COLI_ECUDA;
     const ExpertParams P = expert_params(c, weights, topk_w, y, w8, L, nullptr, nullptr);
@@ -287,7 +292,7 @@ int coli_moe_layer(const coli_moe_cfg* cfg, const coli_moe_weights* weights, con
                           reinterpret_cast<float*>(w8 + L.route_part), reinterpret_cast<uint32_t*>(w8 + L.status),
                           reinterpret_cast<uint32_t*>(w8 + L.status) + 1, stream));
   if (rc) return rc;
-  if (T == 1 && decode_fits(c)) return do_experts(c, weights, T, topk_w, y, w8, L, stream, nullptr, nullptr, x, topk_idx);
+  if (T == 1 && per_row(c) && decode_fits(c)) return do_experts(c, weights, T, topk_w, y, w8, L, stream, nullptr, nullptr, x, topk_idx);
   if ((rc = do_dispatch(c, x, T, topk_idx, w8, L, stream))) return rc;
   return do_experts(c, weights, T, topk_w, y, w8, L, stream, nullptr, nullptr);
 }
@@ -307,7 +312,7 @@ int coli_moe_forward_dump(const coli_moe_cfg* cfg, const coli_moe_weights* weigh
   Layout L;
   if ((rc = check_ws(c, T, ws, ws_bytes, &L))) return rc;
   uint8_t* w8 = static_cast<uint8_t*>(ws);
-  if (T == 1 && decode_fits(c)) return do_experts(c, weights, T, topk_w, y, w8, L, stream, acc_gu, acc_d, x, topk_idx);
+  if (T == 1 && per_row(c) && decode_fits(c)) return do_experts(c, weights, T, topk_w, y, w8, L, stream, acc_gu, acc_d, x, topk_idx);
   if ((rc = do_dispatch(c, x, T, topk_idx, w8, L, stream))) return rc;
   return do_experts(c, weights, T, topk_w, y, w8, L, stream, acc_gu, acc_d);
 }

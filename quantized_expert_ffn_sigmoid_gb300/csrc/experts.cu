@@ -120,6 +120,12 @@ struct BlockW {
   }
 };
 
+// fp32 scales of one expert record: per output row (2 I + H), or per 64
+// weights of a row (gate [I][H/64] | up [I][H/64] | down [H][I/64])
+__device__ __forceinline__ size_t scale_count(const coli_moe_cfg& c, int inter) {
+  return c.group_size ? (size_t)3 * inter * (c.hidden / c.group_size) : (size_t)2 * inter + c.hidden;
+}
+
 __device__ __forceinline__ const uint8_t* entry_record(const ExpertParams& P, int expert, int* inter_out,
                                                        const float** scales_out) {
   const coli_moe_cfg& c = P.cfg;
@@ -127,13 +133,13 @@ __device__ __forceinline__ const uint8_t* entry_record(const ExpertParams& P, in
   if (expert < c.n_experts) {
     const size_t rec = (size_t)2 * c.inter * row_bytes(H, bits) + (size_t)H * row_bytes(c.inter, bits);
     *inter_out = c.inter;
-    *scales_out = P.expert_scales + (size_t)expert * (2 * c.inter + H);
+    *scales_out = P.expert_scales + (size_t)expert * scale_count(c, c.inter);
     return P.experts + (size_t)expert * rec;
   }
   const int s = expert - c.n_experts;
   const size_t rec = (size_t)2 * c.shared_inter * row_bytes(H, bits) + (size_t)H * row_bytes(c.shared_inter, bits);
   *inter_out = c.shared_inter;
-  *scales_out = P.shared_scales + (size_t)s * (2 * c.shared_inter + H);
+  *scales_out = P.shared_scales + (size_t)s * scale_count(c, c.shared_inter);
   return P.shared + (size_t)s * rec;
 }
 
@@ -296,12 +302,20 @@ __device__ void consume_a(const ExpertParams& P, const SmemPtrs& S, const ItemDe
   const int cbytes = BITS == 4 ? 16 : 32;
   uint32_t* status = reinterpret_cast<uint32_t*>(P.ws + P.L.status);
   const int nst = RA / rs;
+  // group-scaled weights: the scale of (row, block cc) is gsc[row * ngr + cc / 2]
+  const int gsz = c.group_size, ngr = gsz ? H / gsz : 0;
+  int e_inter;
+  const float* esc;
+  entry_record(P, d.expert, &e_inter, &esc);
   for (int st = 0; st < nst; ++st, ++stage) {
     const int s = stage % NS;
     mbar_wait(&S.full[s], (stage / NS) & 1u, status);
     const uint8_t* base = S.ring + (size_t)s * SB;
     for (int task = cw; task < ntask; task += NCW) {
       const int rp = task / SA, sp = task % SA;
+      const int grow_i = d.tile * RA + st * rs + rp;
+      const float* gsc_g = esc + (size_t)grow_i * ngr;
+      const float* gsc_u = esc + (size_t)(e_inter + grow_i) * ngr;
       const uint8_t* grow = base + (size_t)rp * rb;
       const uint8_t* urow = base + (size_t)rs * rb + (size_t)rp * rb;
       float pg[TG], pu[TG];
@@ -312,6 +326,8 @@ __device__ void consume_a(const ExpertParams& P, const SmemPtrs& S, const ItemDe
         BlockW<BITS> wg, wu;
         wg.load(grow + (size_t)cc * cbytes);
         wu.load(urow + (size_t)cc * cbytes);
+        const float sgc = gsz ? __ldg(gsc_g + cc * QB / gsz) : 1.0f;
+        const float suc = gsz ? __ldg(gsc_u + cc * QB / gsz) : 1.0f;
 #pragma unroll
         for (int t = 0; t < TG; ++t) {
           if (t < d.ntok) {
@@ -321,8 +337,8 @@ __device__ void consume_a(const ExpertParams& P, const SmemPtrs& S, const ItemDe
             const int ig = wg.dot(a0, a1, corr);
             const int iu = wu.dot(a0, a1, corr);
             const float dv = da[t * nb + cc];
-            pg[t] = fmaf(dv, (float)ig, pg[t]);
-            pu[t] = fmaf(dv, (float)iu, pu[t]);
+            pg[t] = fmaf(__fmul_rn(dv, sgc), (float)ig, pg[t]);
+            pu[t] = fmaf(__fmul_rn(dv, suc), (float)iu, pu[t]);
             if (DUMP && P.dump_gu) {
               const int row = d.tile * RA + st * rs + rp;
               const size_t pbase = (size_t)(d.pair0 + t) * 2 * P.L.imax;
@@ -371,8 +387,9 @@ __device__ void finish_a(const ExpertParams& P, const SmemPtrs& S, const ItemDes
     const float* sc;
     entry_record(P, d.expert, &inter, &sc);
     const int row = d.tile * RA + r;
-    const float g = __fmul_rn(sc[row], gs);
-    const float u = __fmul_rn(sc[inter + row], us);
+    // group-scaled sums already carry their weight scales
+    const float g = c.group_size ? gs : __fmul_rn(sc[row], gs);
+    const float u = c.group_size ? us : __fmul_rn(sc[inter + row], us);
     const float h = __fmul_rn(__fdiv_rn(g, 1.0f + expf(-g)), u);
     float dd;
     bool bad;
@@ -416,6 +433,13 @@ __device__ void consume_b(const ExpertParams& P, const SmemPtrs& S, const ItemDe
   uint32_t* status = reinterpret_cast<uint32_t*>(P.ws + L.status);
   const int H = P.cfg.hidden;
   const int nst = RB / rs;
+  // group-scaled weights: the scale of (down row, block cc) is
+  // esc[2 * I * H / g + row * I / g + cc / (g / 32)]
+  const int gsz = P.cfg.group_size;
+  int e_inter;
+  const float* esc;
+  entry_record(P, d.expert, &e_inter, &esc);
+  const float* gsc_d = gsz ? esc + (size_t)2 * I * (H / gsz) : esc;
   for (int st = 0; st < nst; ++st, ++stage) {
     const int s = stage % NS;
     mbar_wait(&S.full[s], (stage / NS) & 1u, status);
@@ -433,6 +457,11 @@ __device__ void consume_b(const ExpertParams& P, const SmemPtrs& S, const ItemDe
         BlockW<BITS> w[4];
 #pragma unroll
         for (int r = 0; r < 4; ++r) w[r].load(row0 + (size_t)r * rb + (size_t)cc * cbytes);
+        float sdc[4];
+#pragma unroll
+        for (int r = 0; r < 4; ++r)
+          sdc[r] = gsz ? __ldg(gsc_d + (size_t)(d.tile * RB + st * rs + rg * 4 + r) * (I / gsz) + cc * QB / gsz)
+                       : 1.0f;
 #pragma unroll
         for (int t = 0; t < TG; ++t) {
           if (t < d.ntok) {
@@ -443,7 +472,7 @@ __device__ void consume_b(const ExpertParams& P, const SmemPtrs& S, const ItemDe
 #pragma unroll
             for (int r = 0; r < 4; ++r) {
               const int iv = w[r].dot(a0, a1, corr);
-              acc[r][t] = fmaf(dv, (float)iv, acc[r][t]);
+              acc[r][t] = fmaf(__fmul_rn(dv, sdc[r]), (float)iv, acc[r][t]);
               if (DUMP && P.dump_d) {
                 const int row = d.tile * RB + st * rs + rg * 4 + r;
                 P.dump_d[((size_t)(d.pair0 + t) * H + row) * nbI + cc] = iv;
@@ -487,7 +516,7 @@ __device__ void finish_b(const ExpertParams& P, const SmemPtrs& S, const ItemDes
     float sum = 0.f;
     for (int sp = 0; sp < SBk; ++sp) sum += S.red[(r * SBk + sp) * TG + t];
     const int row = d.tile * RB + r;
-    o[(size_t)(d.pair0 + t) * H + row] = __fmul_rn(sc[2 * inter + row], sum);
+    o[(size_t)(d.pair0 + t) * H + row] = c.group_size ? sum : __fmul_rn(sc[2 * inter + row], sum);
   }
   // one acq_rel atomic publishes this CTA's o rows (cumulative release after
   // the barrier) and, for the last arriver, acquires everyone else's
