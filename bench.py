@@ -426,6 +426,7 @@ def secondary(device, b):
                                 "int8_tops": round(ops / (ms / 1e3) / 1e12, 2),
                                 "gbs_min_bytes": round(byt / (ms / 1e3) / 1e9, 1)}
     del xp, ws, idx, w, y
+    res["glm_gs64_decode_b1"] = gs64_bench(device, b)
     res["glm_stack24_mtp1_b32"] = stack_bench(device, b)
     return res
 
@@ -515,6 +516,57 @@ def few_only(args):
     print(json.dumps({"workload": f"{args.only}: GLM-5.2-shaped layer, {T} positions per call, {args.calls} calls",
                       "ms_per_call": round(ms, 4), "tokens_per_s": round(T / (ms / 1e3), 1),
                       "status": cm.coli_moe_status(ws)}), flush=True)
+
+
+def gs64_bench(device, b, calls=300):
+    """The decode workload on group-scaled int4 experts (one fp32 scale per 64
+    weights of a row): 8 rotated copies of the layer, one coli_moe_layer call
+    (one fused launch) per position."""
+    import torch
+    import synth.gpu as sg
+    cm = b.cm
+    shape = synth.GLM_GS64
+    seed = synth.WORKLOADS["glm_decode_b1"][1]
+    cfg = cm.Cfg.of(shape)
+    recs, scs = sg.expert_records(shape, seed, 0, "routed", shape.n_experts, device)
+    srec, ssc = sg.expert_records(shape, seed, 0, "shared", 1, device)
+    wr = torch.from_numpy(synth.router_weight(shape, seed)).to(device)
+    bias = torch.from_numpy(synth.router_bias(shape, seed)).to(device)
+    reps = [(recs, scs, srec, ssc, wr, bias)] + [
+        tuple(a.clone() for a in (recs, scs, srec, ssc, wr, bias)) for _ in range(b.R - 1)]
+    Ws = [cm.make_weights(r[0], r[1], r[2], r[3]) for r in reps]
+    x = sg.token_batch(shape, seed, ("gs64", 0), range(calls), device)
+    ws = cm.new_workspace(cfg, 1)
+    idx = torch.empty((calls, shape.top_k), dtype=torch.int32, device=device)
+    w = torch.empty((calls, shape.top_k), dtype=torch.float32, device=device)
+    y = torch.empty((calls, shape.hidden), dtype=torch.float32, device=device)
+
+    def run():
+        for i in range(calls):
+            r = reps[i % b.R]
+            cm.coli_moe_layer(cfg, Ws[i % b.R], x[i:i + 1], r[4], r[5], idx[i:i + 1], w[i:i + 1],
+                              y[i:i + 1], ws)
+    ms = time_graph(run, 3)
+    rec_bytes = shape.record_bytes() + 4 * shape.scale_count()
+    byt = calls * (9 * rec_bytes + ROUTER_BYTES)
+    out = {"tokens_per_s": round(calls / (ms / 1e3), 1), "us_per_call": round(1e3 * ms / calls, 2),
+           "gbs": round(byt / (ms / 1e3) / 1e9, 1), "bytes_per_call": 9 * rec_bytes + ROUTER_BYTES,
+           "status": cm.coli_moe_status(ws),
+           "note": "group-scaled int4 (gs64), the fused single-position kernel; 8 rotated copies"}
+    del reps, Ws, recs, scs, srec, ssc
+    torch.cuda.empty_cache()
+    return out
+
+
+def gs64_only(args):
+    """--only gs64: the group-scaled decode measurement alone (for profiling)."""
+    import torch
+
+    class _B:  # the two attributes gs64_bench reads
+        import quantized_expert_ffn_sigmoid_gb300 as cm
+        R = REPLICAS
+    print(json.dumps({"workload": "gs64: GLM-5.2-shaped layer, group-scaled int4, decode batch 1",
+                      **gs64_bench(torch.device("cuda", 0), _B)}), flush=True)
 
 
 def stack_bench(device, b, steps=4):
@@ -704,7 +756,7 @@ def main():
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--no-secondary", dest="secondary", action="store_false")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
-    ap.add_argument("--only", choices=["prefill", "mtp", "b32"], default=None,
+    ap.add_argument("--only", choices=["prefill", "mtp", "b32", "gs64"], default=None,
                     help="time one secondary workload alone (profiling)")
     ap.add_argument("--calls", type=int, default=20, help="calls per step of --only mtp / b32")
     ap.add_argument("--prefill-experts", type=int, default=256)
@@ -721,6 +773,8 @@ def main():
         prefill_only(args)
     elif args.only in ("mtp", "b32"):
         few_only(args)
+    elif args.only == "gs64":
+        gs64_only(args)
     else:
         run_gpu(args)
 

@@ -56,8 +56,9 @@ int check_cfg(const coli_moe_cfg* c) {
   return COLI_OK;
 }
 
-// The fast paths take per-row scales; group-scaled weights run on the
-// general expert kernel.
+// The few-position, small-batch and prefill paths take per-row scales;
+// group-scaled weights run on the single-position kernel (which takes both)
+// or else on the general expert kernel.
 bool per_row(const coli_moe_cfg& c) { return c.group_size == 0; }
 
 coli_moe_cfg normalized(const coli_moe_cfg* c) {
@@ -126,7 +127,7 @@ int do_experts(const coli_moe_cfg& c, const coli_moe_weights* w, int T, const fl
                uint8_t* ws, const Layout& L, cudaStream_t st, int32_t* dump_gu, int32_t* dump_d,
                const float* x = nullptr, const int32_t* idx = nullptr) {
   const ExpertParams P = expert_params(c, w, topk_w, y, ws, L, dump_gu, dump_d);
-  if (T == 1 && per_row(c) && decode_fits(c)) {
+  if (T == 1 && decode_fits(c)) {
     const int n_sm = sm_count();
     if (n_sm <= 0) return COLI_ECUDA;
     return rc_of(launch_decode(P, x, idx, x == nullptr, n_sm, st, dump_gu || dump_d));
@@ -260,7 +261,7 @@ int coli_moe_forward(const coli_moe_cfg* cfg, const coli_moe_weights* weights, c
   Layout L;
   if ((rc = check_ws(c, T, ws, ws_bytes, &L))) return rc;
   uint8_t* w8 = static_cast<uint8_t*>(ws);
-  if (T == 1 && per_row(c) && decode_fits(c)) return do_experts(c, weights, T, topk_w, y, w8, L, stream, nullptr, nullptr, x, topk_idx);
+  if (T == 1 && decode_fits(c)) return do_experts(c, weights, T, topk_w, y, w8, L, stream, nullptr, nullptr, x, topk_idx);
   if ((rc = do_dispatch(c, x, T, topk_idx, w8, L, stream))) return rc;
   return do_experts(c, weights, T, topk_w, y, w8, L, stream, nullptr, nullptr);
 }
@@ -281,7 +282,7 @@ int coli_moe_layer(const coli_moe_cfg* cfg, const coli_moe_weights* weights, con
   Layout L;
   if ((rc = check_ws(c, T, ws, ws_bytes, &L))) return rc;
   uint8_t* w8 = static_cast<uint8_t*>(ws);
-  if (T == 1 && per_row(c) && decode_route_fits(c)) {
+  if (T == 1 && decode_route_fits(c)) {
     const int n_sm = sm_count();
     if (n_sm <= 0) return COLI_ECUDA;
     const ExpertParams P = expert_params(c, weights, topk_w, y, w8, L, nullptr, nullptr);
@@ -292,7 +293,7 @@ int coli_moe_layer(const coli_moe_cfg* cfg, const coli_moe_weights* weights, con
                           reinterpret_cast<float*>(w8 + L.route_part), reinterpret_cast<uint32_t*>(w8 + L.status),
                           reinterpret_cast<uint32_t*>(w8 + L.status) + 1, stream));
   if (rc) return rc;
-  if (T == 1 && per_row(c) && decode_fits(c)) return do_experts(c, weights, T, topk_w, y, w8, L, stream, nullptr, nullptr, x, topk_idx);
+  if (T == 1 && decode_fits(c)) return do_experts(c, weights, T, topk_w, y, w8, L, stream, nullptr, nullptr, x, topk_idx);
   if ((rc = do_dispatch(c, x, T, topk_idx, w8, L, stream))) return rc;
   return do_experts(c, weights, T, topk_w, y, w8, L, stream, nullptr, nullptr);
 }
@@ -312,7 +313,7 @@ int coli_moe_forward_dump(const coli_moe_cfg* cfg, const coli_moe_weights* weigh
   Layout L;
   if ((rc = check_ws(c, T, ws, ws_bytes, &L))) return rc;
   uint8_t* w8 = static_cast<uint8_t*>(ws);
-  if (T == 1 && per_row(c) && decode_fits(c)) return do_experts(c, weights, T, topk_w, y, w8, L, stream, acc_gu, acc_d, x, topk_idx);
+  if (T == 1 && decode_fits(c)) return do_experts(c, weights, T, topk_w, y, w8, L, stream, acc_gu, acc_d, x, topk_idx);
   if ((rc = do_dispatch(c, x, T, topk_idx, w8, L, stream))) return rc;
   return do_experts(c, weights, T, topk_w, y, w8, L, stream, acc_gu, acc_d);
 }

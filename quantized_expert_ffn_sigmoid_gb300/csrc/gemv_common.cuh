@@ -59,7 +59,9 @@ __device__ __forceinline__ const uint8_t* gemv_record(const ExpertParams& P, int
   const int e = routed ? expert : expert - c.n_experts;
   const size_t rec = (size_t)2 * I * row_bytes(H, bits) + (size_t)H * row_bytes(I, bits);
   *inter = I;
-  *sc = (routed ? P.expert_scales : P.shared_scales) + (size_t)e * (2 * I + H);
+  // per-row scales (2 I + H per record) or one per 64 weights (3 I H / 64)
+  const size_t nsc = c.group_size ? (size_t)3 * I * (H / c.group_size) : (size_t)2 * I + H;
+  *sc = (routed ? P.expert_scales : P.shared_scales) + (size_t)e * nsc;
   return (routed ? P.experts : P.shared) + (size_t)e * rec;
 }
 

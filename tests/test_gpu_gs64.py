@@ -40,9 +40,11 @@ def test_tiny_gs64_parity(tiny_gs, T):
     check_parity(tiny_gs, x, tiny_gs.run(x))
 
 
-def test_tiny_gs64_layer_call(tiny_gs):
-    # router and experts in one coli_moe_layer call give the split calls' results
-    x, _, _ = margin_batch(tiny_gs.shape, tiny_gs.seed, "gs64layer", 3, tiny_gs.router_w, tiny_gs.bias)
+@pytest.mark.parametrize("T", [1, 3])
+def test_tiny_gs64_layer_call(tiny_gs, T):
+    # router and experts in one coli_moe_layer call (one fused launch at T = 1)
+    # give the split calls' results
+    x, _, _ = margin_batch(tiny_gs.shape, tiny_gs.seed, ("gs64layer", T), T, tiny_gs.router_w, tiny_gs.bias)
     g = tiny_gs.run(x, layer=True)
     check_parity(tiny_gs, x, g)
     assert np.array_equal(g["y"], tiny_gs.run(x, dump=False)["y"])
@@ -65,3 +67,14 @@ def test_glm_gs64_parity(glm_gs, T):
     x, _, _ = margin_batch(glm_gs.shape, glm_gs.seed, ("glm_gs64", T), T, glm_gs.router_w, glm_gs.bias)
     st = check_parity(glm_gs, x, glm_gs.run(x))
     print("gs64 T", T, st)
+
+
+def test_glm_gs64_fused_decode(glm_gs):
+    """One fused launch per position (router inside) on group-scaled experts."""
+    ws = cm.new_workspace(glm_gs.cfg, 1)
+    for p in range(2):
+        x, _, _ = margin_batch(glm_gs.shape, glm_gs.seed, "glm_gs64_layer", 1, glm_gs.router_w, glm_gs.bias,
+                               start=p)
+        g = glm_gs.run(x, layer=True, ws=ws)
+        check_parity(glm_gs, x, g)
+        assert np.array_equal(g["y"], glm_gs.run(x, dump=False, ws=ws)["y"])
