@@ -422,13 +422,45 @@ def secondary(device, b):
     ms = time_graph(pre, 2)
     ops = 2.0 * (T * 8 + T) * 3 * shape.inter * shape.hidden
     byt = (256 + 1) * EXPERT_BYTES + ROUTER_BYTES
+    tops = ops / (ms / 1e3) / 1e12
+    i8 = int8_gemm_tops(device)
+    _, bf16, kind = read_peaks()
     res["glm_prefill_s2048"] = {"tokens_per_s": round(T / (ms / 1e3), 1), "ms_per_call": round(ms, 3),
-                                "int8_tops": round(ops / (ms / 1e3) / 1e12, 2),
-                                "gbs_min_bytes": round(byt / (ms / 1e3) / 1e9, 1)}
+                                "int8_tops": round(tops, 2),
+                                "gbs_min_bytes": round(byt / (ms / 1e3) / 1e9, 1),
+                                "int8_gemm_tops_measured": round(i8, 1),
+                                "frac_of_int8_gemm": round(tops / i8, 3) if i8 else None,
+                                "frac_of_bf16_peak": round(tops / bf16, 4),
+                                "peak_note": "int8: the library int8 GEMM (cuBLASLt through torch._int_mm, 8192^3) "
+                                             "on this GPU, which has no tcgen05 int8 MMA; bf16: " + kind +
+                                             " dense bf16, the rate of the kind::f16 MMA the kernel uses"}
     del xp, ws, idx, w, y
     res["glm_gs64_decode_b1"] = gs64_bench(device, b)
     res["glm_stack24_mtp1_b32"] = stack_bench(device, b)
     return res
+
+
+def int8_gemm_tops(device, n=8192, reps=3):
+    """Measured int8 tensor throughput of the library GEMM (int8 x int8 -> int32,
+    n^3), the reference point for the prefill's int8-equivalent rate."""
+    import torch
+    try:
+        a = torch.randint(-127, 128, (n, n), dtype=torch.int8, device=device)
+        b = torch.randint(-127, 128, (n, n), dtype=torch.int8, device=device)
+        torch._int_mm(a, b)
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(reps):
+            torch._int_mm(a, b)
+        e1.record()
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / reps
+        del a, b
+        return 2.0 * n ** 3 / (ms / 1e3) / 1e12
+    except (RuntimeError, AttributeError):
+        return 0.0
 
 
 def prefill_only(args):
