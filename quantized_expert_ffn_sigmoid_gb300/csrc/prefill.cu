@@ -475,11 +475,18 @@ __global__ void __launch_bounds__(PF_THREADS2, 1) pf_gemm(const __grid_constant_
           const uint32_t tbase = taddr + ((uint32_t)(32 * q4) << 16) + b * BUFCOLS + (uint32_t)(cg * PF_EPC);
           constexpr int NA = PF_CB * NW;  // accumulators of this chunk
           constexpr int BATCH = NA >= 2 ? 2 : 1;  // loads in flight per wait
+          static_assert(NW == 1 || BATCH == NW, "a batch is the gate and up accumulators of one block");
 #pragma unroll
           for (int a0 = 0; a0 < NA; a0 += BATCH) {
             uint32_t v[BATCH][PF_EPC];
 #pragma unroll
             for (int i = 0; i < BATCH; ++i) tmem_ld16_nowait(tbase + (uint32_t)((a0 + i) * 64), v[i]);
+            // this thread's column scales of the batch's first block, read once
+            // for gate and up (the same block)
+            float4 dq[PF_EPC / 4];
+#pragma unroll
+            for (int j4 = 0; j4 < PF_EPC / 4; ++j4)
+              dq[j4] = reinterpret_cast<const float4*>(&s_dxr[ch % PF_DXR][a0 / NW][cg * PF_EPC])[j4];
             tmem_wait_ld();
 #pragma unroll
             for (int i = 0; i < BATCH; ++i) {
@@ -487,7 +494,7 @@ __global__ void __launch_bounds__(PF_THREADS2, 1) pf_gemm(const __grid_constant_
               const float4* d4 = reinterpret_cast<const float4*>(&s_dxr[ch % PF_DXR][blk][cg * PF_EPC]);
 #pragma unroll
               for (int j4 = 0; j4 < PF_EPC / 4; ++j4) {
-                const float4 d = d4[j4];
+                const float4 d = NW == 2 ? dq[j4] : d4[j4];
                 ffma2(acc[m][4 * j4], acc[m][4 * j4 + 1], d.x, d.y, __uint_as_float(v[i][4 * j4]),
                       __uint_as_float(v[i][4 * j4 + 1]));
                 ffma2(acc[m][4 * j4 + 2], acc[m][4 * j4 + 3], d.z, d.w, __uint_as_float(v[i][4 * j4 + 2]),
