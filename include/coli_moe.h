@@ -79,7 +79,8 @@ typedef struct coli_moe_cfg {
     int32_t weight_bits;            /* 4: packed int4, 8: int8              */
     float   routed_scaling_factor;  /* multiplies the renormalised weights  */
     int32_t group_size;             /* 0: one scale per output row;
-                                       64: one per 64 weights of a row ("gs64") */
+                                       64: one per 64 weights of a row ("gs64",
+                                       int4 only: COLI_EUNSUPPORTED with int8) */
 } coli_moe_cfg;
 
 /* Expert weights.  One expert "record" is its three matrices stored adjacent

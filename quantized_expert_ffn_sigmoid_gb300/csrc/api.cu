@@ -47,6 +47,7 @@ int check_cfg(const coli_moe_cfg* c) {
   if (c->n_shared > 0 && (c->shared_inter <= 0 || c->shared_inter % 128)) return COLI_EINVAL;
   if (c->weight_bits != 4 && c->weight_bits != 8) return COLI_EINVAL;
   if (c->group_size != 0 && c->group_size != 64) return COLI_EINVAL;
+  if (c->group_size != 0 && c->weight_bits != 4) return COLI_EUNSUPPORTED;  // group scales: int4 only
   if (!(c->routed_scaling_factor == c->routed_scaling_factor)) return COLI_EINVAL;
   // a gate+up stage must hold at least one row pair, a down stage four rows
   if (2 * row_bytes(c->hidden, c->weight_bits) > SB) return COLI_EUNSUPPORTED;

@@ -66,3 +66,17 @@ def test_host_only_entry_points(lib):
     bad = cm.Cfg.of(synth.GLM)
     bad.top_k = 40
     assert cm.coli_moe_workspace_size(bad, 4) == 0
+
+
+def test_group_size_host_checks(lib):
+    # group scales: 0 (per row) or 64, and only with int4 codes
+    import dataclasses
+    import synth
+    import quantized_expert_ffn_sigmoid_gb300 as cm
+    gs = cm.Cfg.of(synth.GLM_GS64)
+    assert gs.group_size == 64
+    assert cm.coli_moe_workspace_size(gs, 4) == cm.coli_moe_workspace_size(cm.Cfg.of(synth.GLM), 4) > 0
+    for bad in (dataclasses.replace(synth.GLM_GS64, group_size=32),
+                dataclasses.replace(synth.GLM_GS64, weight_bits=8)):
+        assert cm.coli_moe_workspace_size(cm.Cfg.of(bad), 4) == 0
+    assert cm.Cfg.of(synth.GLM).group_size == 0
