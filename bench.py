@@ -436,6 +436,7 @@ def secondary(device, b):
                                              " dense bf16, the rate of the kind::f16 MMA the kernel uses"}
     del xp, ws, idx, w, y
     res["glm_gs64_decode_b1"] = gs64_bench(device, b)
+    res["glm_gs64_mtp_verify_t4"] = gs64_bench(device, b, calls=100, T=4)
     res["glm_stack24_mtp1_b32"] = stack_bench(device, b)
     return res
 
@@ -550,7 +551,7 @@ def few_only(args):
                       "status": cm.coli_moe_status(ws)}), flush=True)
 
 
-def gs64_bench(device, b, calls=300):
+def gs64_bench(device, b, calls=300, T=1):
     """The decode workload on group-scaled int4 experts (one fp32 scale per 64
     weights of a row): 8 rotated copies of the layer, one coli_moe_layer call
     (one fused launch) per position."""
@@ -567,24 +568,35 @@ def gs64_bench(device, b, calls=300):
     reps = [(recs, scs, srec, ssc, wr, bias)] + [
         tuple(a.clone() for a in (recs, scs, srec, ssc, wr, bias)) for _ in range(b.R - 1)]
     Ws = [cm.make_weights(r[0], r[1], r[2], r[3]) for r in reps]
-    x = sg.token_batch(shape, seed, ("gs64", 0), range(calls), device)
-    ws = cm.new_workspace(cfg, 1)
-    idx = torch.empty((calls, shape.top_k), dtype=torch.int32, device=device)
-    w = torch.empty((calls, shape.top_k), dtype=torch.float32, device=device)
-    y = torch.empty((calls, shape.hidden), dtype=torch.float32, device=device)
+    if T == 1:
+        x = sg.token_batch(shape, seed, ("gs64", 0), range(calls), device).view(calls, 1, -1)
+    else:  # the MTP-verify chain: T correlated positions per call
+        mseed = synth.WORKLOADS["glm_mtp_verify_t4"][1]
+        x = torch.from_numpy(np.stack([synth.mtp_chain(shape, mseed, c, n_pos=T) for c in range(calls)])).to(device)
+    ws = cm.new_workspace(cfg, T)
+    idx = torch.empty((calls, T, shape.top_k), dtype=torch.int32, device=device)
+    w = torch.empty((calls, T, shape.top_k), dtype=torch.float32, device=device)
+    y = torch.empty((calls, T, shape.hidden), dtype=torch.float32, device=device)
+    L = cm.coli_moe_workspace_layout(cfg, T)
+    uniq = 0
+    for i in range(calls):
+        r = reps[i % b.R]
+        cm.coli_moe_layer(cfg, Ws[i % b.R], x[i], r[4], r[5], idx[i], w[i], y[i], ws)
+        uniq += int(ws[L.n_entries:L.n_entries + 4].view(torch.int32).item())  # routed + shared
 
     def run():
         for i in range(calls):
             r = reps[i % b.R]
-            cm.coli_moe_layer(cfg, Ws[i % b.R], x[i:i + 1], r[4], r[5], idx[i:i + 1], w[i:i + 1],
-                              y[i:i + 1], ws)
+            cm.coli_moe_layer(cfg, Ws[i % b.R], x[i], r[4], r[5], idx[i], w[i], y[i], ws)
     ms = time_graph(run, 3)
     rec_bytes = shape.record_bytes() + 4 * shape.scale_count()
-    byt = calls * (9 * rec_bytes + ROUTER_BYTES)
-    out = {"tokens_per_s": round(calls / (ms / 1e3), 1), "us_per_call": round(1e3 * ms / calls, 2),
-           "gbs": round(byt / (ms / 1e3) / 1e9, 1), "bytes_per_call": 9 * rec_bytes + ROUTER_BYTES,
+    byt = uniq * rec_bytes + calls * ROUTER_BYTES
+    out = {"tokens_per_s": round(T * calls / (ms / 1e3), 1), "us_per_call": round(1e3 * ms / calls, 2),
+           "gbs": round(byt / (ms / 1e3) / 1e9, 1), "experts_per_call": round(uniq / calls, 2),
            "status": cm.coli_moe_status(ws),
-           "note": "group-scaled int4 (gs64), the fused single-position kernel; 8 rotated copies"}
+           "note": ("group-scaled int4 (gs64), the fused single-position kernel" if T == 1 else
+                    "group-scaled int4 (gs64) at 4 positions per call, the general expert kernel") +
+                   "; 8 rotated copies"}
     del reps, Ws, recs, scs, srec, ssc
     torch.cuda.empty_cache()
     return out
@@ -597,8 +609,10 @@ def gs64_only(args):
     class _B:  # the two attributes gs64_bench reads
         import quantized_expert_ffn_sigmoid_gb300 as cm
         R = REPLICAS
-    print(json.dumps({"workload": "gs64: GLM-5.2-shaped layer, group-scaled int4, decode batch 1",
-                      **gs64_bench(torch.device("cuda", 0), _B)}), flush=True)
+    for T in (1, 4):
+        print(json.dumps({"workload": f"gs64: GLM-5.2-shaped layer, group-scaled int4, {T} position(s) per call",
+                          **gs64_bench(torch.device("cuda", 0), _B, calls=300 if T == 1 else 100, T=T)}),
+              flush=True)
 
 
 def stack_bench(device, b, steps=4):
