@@ -78,3 +78,43 @@ def test_glm_gs64_fused_decode(glm_gs):
         g = glm_gs.run(x, layer=True, ws=ws)
         check_parity(glm_gs, x, g)
         assert np.array_equal(g["y"], glm_gs.run(x, dump=False, ws=ws)["y"])
+
+
+def test_gs64_given_routing_edge_cases(tiny_gs):
+    """Duplicate ids, skipped slots and an all-skipped position, at several
+    positions per call and at one (the single-position kernel)."""
+    x = synth.token_batch(tiny_gs.shape, 17, 0, range(5))
+    idx = np.array([[0, 3, 3, 7], [15, -1, 2, -1], [1, 2, 5, 6], [-1, -1, -1, -1], [4, 4, 4, 4]])
+    w = np.array([[0.5, 0.25, 0.25, 0.0], [1.0, 9.0, 0.0, 9.0], [1.0, 0.0, 0.0, 0.0],
+                  [0.0, 0.0, 0.0, 0.0], [0.1, 0.2, 0.3, 0.4]], np.float32)
+    g = tiny_gs.run(x, route=False, idx=idx, w=w)
+    check_parity(tiny_gs, x, g, idx=idx, w=w.astype(np.float64))
+    for p in (0, 3, 4):
+        g1 = tiny_gs.run(x[p:p + 1], route=False, idx=idx[p:p + 1], w=w[p:p + 1])
+        check_parity(tiny_gs, x[p:p + 1], g1, idx=idx[p:p + 1], w=w[p:p + 1].astype(np.float64))
+
+
+@pytest.mark.parametrize("n_shared,shared_inter", [(0, 128), (2, 256)])
+def test_gs64_shared_expert_variants(n_shared, shared_inter):
+    import dataclasses
+    shape = dataclasses.replace(synth.TINY_GS64, n_shared=n_shared, shared_inter=shared_inter)
+    L = DeviceLayer(shape, 27)
+    for T in (1, 6):
+        x, _, _ = margin_batch(shape, 27, ("gs64sh", T), T, L.router_w, L.bias)
+        check_parity(L, x, L.run(x))
+
+
+def test_gs64_nonfinite_and_empty(tiny_gs):
+    x = synth.token_batch(tiny_gs.shape, 18, 0, range(2))
+    xn = x.copy()
+    xn[1, 9] = np.nan
+    g = tiny_gs.run(xn, dump=False)
+    assert g["status"] & cm.STATUS_NONFINITE
+    assert (g["idx"][1] == -1).all() and (g["w"][1] == 0).all()
+    ws = cm.new_workspace(tiny_gs.cfg, 2)
+    xd = torch.zeros((0, tiny_gs.shape.hidden), device="cuda")
+    idx = torch.zeros((0, tiny_gs.shape.top_k), dtype=torch.int32, device="cuda")
+    w = torch.zeros((0, tiny_gs.shape.top_k), device="cuda")
+    y = torch.zeros((0, tiny_gs.shape.hidden), device="cuda")
+    cm.coli_moe_layer(tiny_gs.cfg, tiny_gs.W, xd, tiny_gs.wr_d, tiny_gs.bias_d, idx, w, y, ws)
+    assert cm.coli_moe_status(ws) == 0
