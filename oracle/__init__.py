@@ -13,8 +13,8 @@ It computes the layer literally, following the colibrì pages:
   weights renormalised from the unbiased sigmoid, non-finite input rejected;
   plus the group-limited top-k of the DeepSeek-V3 ``noaux_tc`` pattern that
   the same page and the colibrì v1.0 README ("What's implemented") name.
-* Q8_0-style activations, packed int4 / int8 per-row-scaled weights, the
-  SwiGLU expert and the batch-union evaluation -- colibrì v1.0 README,
+* Q8_0-style activations, packed int4 / packed int2 / int8 per-row-scaled
+  weights, the SwiGLU expert and the batch-union evaluation -- colibrì v1.0 README,
   "What's implemented" (integer-dot kernels, quantization kernels,
   batch-union MoE) and "Experimental Metal backend" (routed-expert SwiGLU).
 * the routing-weighted combine plus the always-on shared expert -- the
@@ -32,14 +32,15 @@ printed worked example on the pages and are pinned only through those
 invariants and the fp64 dequantised bound.
 """
 from .quant import (q8_0_quantize, q8_0_dequantize, q8_0_stable_mask,
-                    int4_pack, int4_unpack, unpack_weight_rows)
+                    int4_pack, int4_unpack, int2_pack, int2_unpack,
+                    unpack_weight_rows)
 from .router import (router_logits, route, route_margins, sigmoid)
 from .expert import block_dots, expert_ffn, expert_ffn_dequant_fp64
 from .layer import (union_tables, moe_forward, moe_layer, dense_reference)
 
 __all__ = [
     "q8_0_quantize", "q8_0_dequantize", "q8_0_stable_mask", "int4_pack",
-    "int4_unpack", "unpack_weight_rows", "router_logits", "route",
+    "int4_unpack", "int2_pack", "int2_unpack", "unpack_weight_rows", "router_logits", "route",
     "route_margins", "sigmoid", "block_dots", "expert_ffn",
     "expert_ffn_dequant_fp64", "union_tables", "moe_forward", "moe_layer",
     "dense_reference",

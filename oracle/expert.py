@@ -3,7 +3,8 @@
 TEST INFRASTRUCTURE ONLY (see the package docstring).
 
 Source: colibrì v1.0 README, "What's implemented" (integer-dot kernels on
-Q8_0-style int8 activations; int8 / packed int4 weights with per-row scales)
+Q8_0-style int8 activations; int8 / packed int4 / packed int2 weights with
+per-row scales)
 and "Experimental Metal backend" (the routed-expert SwiGLU).  Group-scaled
 int4 ("gs64": one scale per 64 weights of a row instead of one per row) is the
 container the colibri GLM-5.2 quick start recommends ("2. Get the model").
@@ -84,7 +85,7 @@ def _split_scales(scales, H: int, I: int, group: int):
 
 
 def _split_record(record: np.ndarray, H: int, I: int, bits: int):
-    rb = (lambda k: k // 2) if bits == 4 else (lambda k: k)
+    rb = {2: lambda k: k // 4, 4: lambda k: k // 2, 8: lambda k: k}[bits]
     n_gu = I * rb(H)
     n_d = H * rb(I)
     rec = np.asarray(record, np.uint8).reshape(-1)

@@ -3,9 +3,9 @@
 TEST INFRASTRUCTURE ONLY (see the package docstring).
 
 Source: colibrì v1.0 README, section "What's implemented" -- integer-dot
-kernels with "Q8_0-style" int8 activations, and quantization kernels for int8
-and packed int4 weights with per-row scales, dequantised on use, whose packing
-is checked to be bit-identical to the int8 container.
+kernels with "Q8_0-style" int8 activations, and quantization kernels for int8,
+packed int4 and packed int2 weights with per-row scales, dequantised on use,
+whose packing is checked to be bit-identical to the int8 container.
 
 The pages name the format but print no definition.  Readings taken here:
 
@@ -17,6 +17,9 @@ The pages name the format but print no definition.  Readings taken here:
 * packed int4: row-major, byte j of a row holds element 2j in the low nibble
   and element 2j+1 in the high nibble, each stored offset-binary (code + 8),
   so the codes span [-8, 7].
+* packed int2: row-major, byte j of a row holds elements 4j .. 4j+3, element
+  4j+m in bits 2m and 2m+1 (lowest element in the lowest bits, as for int4),
+  each stored offset-binary (code + 2), so the codes span [-2, 1].
 """
 from __future__ import annotations
 
@@ -111,11 +114,36 @@ def int4_unpack(b: np.ndarray) -> np.ndarray:
     return out
 
 
+def int2_pack(q: np.ndarray) -> np.ndarray:
+    """Pack int2 codes ``q[..., K]`` (values in [-2, 1], K % 4 == 0) to bytes."""
+    q = np.asarray(q)
+    if q.shape[-1] % 4:
+        raise ValueError("K must be a multiple of 4")
+    if q.min(initial=0) < -2 or q.max(initial=0) > 1:
+        raise ValueError("int2 code out of range")
+    n = (q.astype(np.int16) + 2).astype(np.uint8)
+    b = np.zeros(q.shape[:-1] + (q.shape[-1] // 4,), np.uint8)
+    for m in range(4):
+        b |= (n[..., m::4] << (2 * m)).astype(np.uint8)
+    return b
+
+
+def int2_unpack(b: np.ndarray) -> np.ndarray:
+    """Unpack bytes ``b[..., K/4]`` to int2 codes ``[..., K]`` (int8)."""
+    b = np.asarray(b, dtype=np.uint8)
+    out = np.empty(b.shape[:-1] + (4 * b.shape[-1],), np.int8)
+    for m in range(4):
+        out[..., m::4] = ((b >> (2 * m)) & 3).astype(np.int16) - 2
+    return out
+
+
 def unpack_weight_rows(raw: np.ndarray, rows: int, k: int, bits: int) -> np.ndarray:
     """Weight codes [rows, k] from a row-major packed matrix of ``bits`` bits."""
     raw = np.asarray(raw, np.uint8)
     if bits == 4:
         return int4_unpack(raw.reshape(rows, k // 2))
+    if bits == 2:
+        return int2_unpack(raw.reshape(rows, k // 4))
     if bits == 8:
         return raw.reshape(rows, k).view(np.int8)
-    raise ValueError("weight_bits must be 4 or 8")
+    raise ValueError("weight_bits must be 2, 4 or 8")

@@ -23,7 +23,9 @@ Value recipes (the workload descriptions name normal distributions):
   multiply, round to nearest).
 * quantised weights (per-row absmax): ``q = sign(z)*floor((2*qmax*|z| +
   amax)/(2*amax))`` (round half away from zero of ``qmax*z/amax``, exact in
-  integers) and ``scale = float32(float64(amax) * (std/(SIGMA_Z*qmax)))``.
+  integers) and ``scale = float32(float64(amax) * (std/(SIGMA_Z*qmax)))``;
+  qmax is 7 for int4, 127 for int8 and 2 for int2, whose codes are then
+  clamped to the container's [-2, 1] (so every one of the four codes occurs).
 * uniform fp32 in (lo, hi): ``float32(lo + (hi-lo)*(r0+0.5)/2**32)``.
 """
 from __future__ import annotations
@@ -171,6 +173,21 @@ def quantize_groups_int(z: np.ndarray, qmax: int, group: int):
     return q.reshape(rows, k), amax.reshape(rows, k // group)
 
 
+def pack_int2_rows(q: np.ndarray) -> np.ndarray:
+    """Pack signed int2 codes [rows, K] into bytes [rows, K/4].
+
+    Byte j of a row holds elements 4j .. 4j+3, element 4j+m in bits 2m and
+    2m+1, each stored offset-binary (code + 2)."""
+    n = (q.astype(np.int16) + 2).astype(np.uint8)
+    b = np.zeros((q.shape[0], q.shape[1] // 4), np.uint8)
+    for m in range(4):
+        b |= (n[:, m::4] << (2 * m)).astype(np.uint8)
+    return b
+
+
+INT2_LO, INT2_HI = -2, 1
+
+
 def scale_from_amax(amax: np.ndarray, std: float, qmax: int) -> np.ndarray:
     c = std / (SIGMA_Z * qmax)
     return (amax.astype(np.float64) * c).astype(np.float32)
@@ -201,10 +218,10 @@ class LayerShape:
 
     @property
     def qmax(self) -> int:
-        return 7 if self.weight_bits == 4 else 127
+        return {2: 2, 4: 7, 8: 127}[self.weight_bits]
 
     def row_bytes(self, k: int) -> int:
-        return k // 2 if self.weight_bits == 4 else k
+        return k * self.weight_bits // 8
 
     def record_bytes(self, inter: int | None = None) -> int:
         i = self.inter if inter is None else inter
@@ -241,7 +258,13 @@ def expert_matrix(shape: LayerShape, seed, layer, kind, expert, matrix):
     else:
         q, amax = quantize_rows_int(z, shape.qmax)
         scales = scale_from_amax(amax, WEIGHT_STD, shape.qmax)
-    packed = pack_int4_rows(q) if shape.weight_bits == 4 else q.view(np.uint8)
+    if shape.weight_bits == 2:
+        q = np.clip(q, INT2_LO, INT2_HI).astype(np.int8)
+        packed = pack_int2_rows(q)
+    elif shape.weight_bits == 4:
+        packed = pack_int4_rows(q)
+    else:
+        packed = q.view(np.uint8)
     return q, packed, scales
 
 
@@ -324,6 +347,13 @@ TINY_GS64 = LayerShape(hidden=256, n_experts=16, n_groups=4, topk_group=2, top_k
 GLM_GS64 = LayerShape(hidden=6144, n_experts=256, n_groups=8, topk_group=4, top_k=8,
                       inter=2048, n_shared=1, shared_inter=2048, weight_bits=4,
                       routed_scaling_factor=2.5, group_size=64)
+# packed int2 experts (per-row scales)
+TINY_INT2 = LayerShape(hidden=256, n_experts=16, n_groups=4, topk_group=2, top_k=4,
+                       inter=128, n_shared=1, shared_inter=128, weight_bits=2,
+                       routed_scaling_factor=2.5)
+GLM_INT2 = LayerShape(hidden=6144, n_experts=256, n_groups=8, topk_group=4, top_k=8,
+                      inter=2048, n_shared=1, shared_inter=2048, weight_bits=2,
+                      routed_scaling_factor=2.5)
 
 WORKLOADS = {
     # name: (shape, seed, positions per call, calls)

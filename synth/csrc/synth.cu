@@ -1,7 +1,7 @@
 // Device twin of the seeded input generator in synth/__init__.py:
 // Philox4x32-10 (Salmon et al., SC'11) keyed per tensor, Irwin-Hall sums of
 // four 16-bit uniforms, per-row (or per-64-element) absmax integer
-// quantisation and int4 packing.
+// quantisation and int4 / int2 packing.
 // Every step is integer arithmetic except one IEEE double multiply and one
 // round-to-nearest conversion per scale, so it matches the numpy version bit
 // for bit.  Holds none of the MoE layer's arithmetic.
@@ -56,15 +56,28 @@ __global__ void __launch_bounds__(256) quant_rows_kernel(uint32_t k0, uint32_t k
     int amax = 0;
     for (int w = 0; w < (int)(blockDim.x >> 5); ++w) amax = max(amax, red[w]);
     __syncthreads();
-    for (int j = threadIdx.x; j < half; j += blockDim.x) {
-      int z0, z1;
-      pair_normals(base + j, k0, k1, &z0, &z1);
-      const int q0 = quant(z0, amax, qmax), q1 = quant(z1, amax, qmax);
-      if (bits == 4) {
-        out[(size_t)row * half + j] = (uint8_t)((q0 + 8) | ((q1 + 8) << 4));
-      } else {
-        out[(size_t)row * K + 2 * j] = (uint8_t)(int8_t)q0;
-        out[(size_t)row * K + 2 * j + 1] = (uint8_t)(int8_t)q1;
+    if (bits == 2) {
+      // one byte per four elements (two draws), codes clamped to [-2, 1]
+      for (int j = threadIdx.x; j < K / 4; j += blockDim.x) {
+        int z[4];
+        pair_normals(base + 2 * j, k0, k1, &z[0], &z[1]);
+        pair_normals(base + 2 * j + 1, k0, k1, &z[2], &z[3]);
+        uint32_t b = 0;
+#pragma unroll
+        for (int m = 0; m < 4; ++m) b |= (uint32_t)(min(quant(z[m], amax, qmax), 1) + 2) << (2 * m);
+        out[(size_t)row * (K / 4) + j] = (uint8_t)b;
+      }
+    } else {
+      for (int j = threadIdx.x; j < half; j += blockDim.x) {
+        int z0, z1;
+        pair_normals(base + j, k0, k1, &z0, &z1);
+        const int q0 = quant(z0, amax, qmax), q1 = quant(z1, amax, qmax);
+        if (bits == 4) {
+          out[(size_t)row * half + j] = (uint8_t)((q0 + 8) | ((q1 + 8) << 4));
+        } else {
+          out[(size_t)row * K + 2 * j] = (uint8_t)(int8_t)q0;
+          out[(size_t)row * K + 2 * j + 1] = (uint8_t)(int8_t)q1;
+        }
       }
     }
     if (threadIdx.x == 0) scales[row] = __double2float_rn((double)amax * c);
@@ -113,10 +126,10 @@ __global__ void normal_f32_kernel(uint32_t k0, uint32_t k1, long long n, float m
 
 extern "C" {
 
-// Quantised weight matrix [rows][K]: bytes (int4 packed or int8) and scales.
+// Quantised weight matrix [rows][K]: bytes (int4 / int2 packed or int8) and scales.
 int synth_quant_rows(uint32_t k0, uint32_t k1, int rows, int K, int qmax, double c, int bits, void* out,
                      float* scales, cudaStream_t st) {
-  if (K % 2 || rows <= 0) return -1;
+  if (K % 2 || rows <= 0 || (bits == 2 && K % 4)) return -1;
   int grid = rows < 4096 ? rows : 4096;
   quant_rows_kernel<<<grid, 256, 0, st>>>(k0, k1, rows, K, qmax, c, bits, static_cast<uint8_t*>(out), scales);
   return cudaGetLastError() == cudaSuccess ? 0 : -2;
@@ -125,7 +138,7 @@ int synth_quant_rows(uint32_t k0, uint32_t k1, int rows, int K, int qmax, double
 // The same with one scale per 64 elements of a row (K a multiple of 64).
 int synth_quant_groups64(uint32_t k0, uint32_t k1, int rows, int K, int qmax, double c, int bits, void* out,
                          float* scales, cudaStream_t st) {
-  if (K % 64 || rows <= 0) return -1;
+  if (K % 64 || rows <= 0 || bits == 2) return -1;
   const long long warps = (long long)rows * (K / 64);
   const long long blocks = (warps + 7) / 8 < 65536 ? (warps + 7) / 8 : 65536;
   quant_groups64_kernel<<<(unsigned)blocks, 256, 0, st>>>(k0, k1, rows, K, qmax, c, bits, static_cast<uint8_t*>(out),

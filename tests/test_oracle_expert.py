@@ -30,7 +30,8 @@ def test_block_dot_brute_force():
 
 
 def _record(gate, up, down, bits=4):
-    pk = oracle.int4_pack if bits == 4 else (lambda q: q.astype(np.int8).view(np.uint8))
+    pk = {4: oracle.int4_pack, 2: oracle.int2_pack,
+          8: lambda q: q.astype(np.int8).view(np.uint8)}[bits]
     return np.concatenate([pk(gate).reshape(-1), pk(up).reshape(-1), pk(down).reshape(-1)])
 
 
@@ -86,9 +87,49 @@ def test_zero_expert_gives_zero():
     assert np.all(out["o"] == 0) and np.all(out["qh"] == 0) and np.all(out["dh"] == 0)
 
 
-@pytest.mark.parametrize("bits", [4, 8])
+def test_int2_expert_closed_form():
+    # H = I = 32, gate codes -2, up codes 1, down codes alternating -2 / 1,
+    # scales 1, x all 1 (qx = 127, dx = 1/127): g = -2 * 32 = -64, u = 32,
+    # h = silu(-64) * 32 (tiny, negative, all equal -> qh = -127),
+    # o[c] = dh * (-127) * sum(down row c) = dh * (-127) * 16 * (-1)
+    H = I = 32
+    gate = np.full((I, H), -2, np.int8)
+    up = np.ones((I, H), np.int8)
+    down = np.tile(np.array([-2, 1], np.int8), (H, I // 2))
+    rec = _record(gate, up, down, bits=2)
+    assert rec.size == 3 * 32 * 32 // 4
+    scales = np.ones(2 * I + H, np.float32)
+    qx, dx = oracle.q8_0_quantize(np.ones((1, H), np.float32))
+    out = oracle.expert_ffn(rec, scales, H, I, 2, qx, dx)
+    assert np.all(out["acc_g"] == -2 * 32 * 127) and np.all(out["acc_u"] == 32 * 127)
+    d = float(np.float32(1.0) / np.float32(127.0))
+    g, u = -2 * 32 * 127 * d, 32 * 127 * d
+    h = g / (1 + np.exp(-g)) * u
+    assert np.allclose(out["h"], h, rtol=1e-15)
+    assert np.all(out["qh"] == -127)
+    assert np.all(out["acc_d"] == -127 * 16 * (-2 + 1))
+    dh = float(np.float32(np.float32(abs(h)) / np.float32(127)))
+    assert np.allclose(out["o"], dh * 127 * 16, rtol=1e-12)
+
+
+def test_int2_expert_equals_int8_container():
+    # the same codes through the int2 and the int8 containers give identical results
+    rng = np.random.default_rng(5)
+    H, I = 64, 32
+    gate, up = rng.integers(-2, 2, (I, H)), rng.integers(-2, 2, (I, H))
+    down = rng.integers(-2, 2, (H, I))
+    scales = rng.uniform(0.01, 0.1, 2 * I + H).astype(np.float32)
+    qx, dx = oracle.q8_0_quantize(rng.standard_normal((3, H)).astype(np.float32))
+    a = oracle.expert_ffn(_record(gate, up, down, 2), scales, H, I, 2, qx, dx)
+    b = oracle.expert_ffn(_record(gate, up, down, 8), scales, H, I, 8, qx, dx)
+    for key in ("acc_g", "acc_u", "acc_d", "qh", "dh", "o"):
+        assert np.array_equal(a[key], b[key]), key
+
+
+@pytest.mark.parametrize("bits", [2, 4, 8])
 def test_expert_matches_fp64_dequantised_products(bits):
-    shape = synth.TINY if bits == 4 else synth.LayerShape(256, 16, 4, 2, 4, 128, 1, 128, 8, 2.5)
+    shape = {4: synth.TINY, 2: synth.TINY_INT2,
+             8: synth.LayerShape(256, 16, 4, 2, 4, 128, 1, 128, 8, 2.5)}[bits]
     rec, sc = synth.expert_record(shape, 11, 0, "routed", 3)
     x = synth.token_batch(shape, 11, 0, range(6))
     qx, dx = oracle.q8_0_quantize(x)

@@ -1,4 +1,4 @@
-"""Pins for the oracle's Q8_0 and int4 code paths (hand-worked blocks,
+"""Pins for the oracle's Q8_0, int4 and int2 code paths (hand-worked blocks,
 closed forms and invariants)."""
 import json
 import os
@@ -75,6 +75,35 @@ def test_int4_round_trip_all_codes_and_int8_container():
     assert np.array_equal(rows, rows8)
     with pytest.raises(ValueError):
         oracle.int4_pack(np.array([9, 0]))
+
+
+def test_int2_pack_hand_worked():
+    cases = json.load(open(os.path.join(GOLD, "int2_pack.json")))["cases"]
+    for c in cases:
+        b = oracle.int2_pack(np.array(c["codes"]))
+        assert b.tolist() == c["bytes"]
+        assert oracle.int2_unpack(np.array(c["bytes"], np.uint8)).tolist() == c["codes"]
+
+
+def test_int2_round_trip_all_codes_and_int8_container():
+    # every byte value once: 256 bytes hold all 4^4 code quadruples
+    codes = np.array([[(v >> (2 * m) & 3) - 2 for m in range(4)] for v in range(256)]).reshape(1, -1)
+    b = oracle.int2_pack(codes)
+    assert b.reshape(-1).tolist() == list(range(256))
+    assert np.array_equal(oracle.int2_unpack(b), codes)
+    rows = oracle.unpack_weight_rows(b.reshape(-1), 1, codes.shape[1], 2)
+    rows8 = oracle.unpack_weight_rows(codes.astype(np.int8).view(np.uint8).reshape(-1), 1,
+                                      codes.shape[1], 8)
+    assert np.array_equal(rows, rows8)
+    # element i of a row sits in byte i // 4 at bit 2 * (i % 4)
+    one = np.full((1, 32), -2)
+    one[0, 13] = 1
+    bb = oracle.int2_pack(one)[0]
+    assert bb.tolist() == [0, 0, 0, 3 << 2, 0, 0, 0, 0]
+    with pytest.raises(ValueError):
+        oracle.int2_pack(np.array([2, 0, 0, 0]))
+    with pytest.raises(ValueError):
+        oracle.int2_pack(np.array([0, 0]))
 
 
 def test_stable_mask_flags_boundaries():

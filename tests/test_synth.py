@@ -36,6 +36,20 @@ def test_weight_recipe_packs_like_oracle_unpacks():
         assert scales.dtype == np.float32 and np.all(scales > 0)
 
 
+def test_int2_recipe_packs_like_oracle_unpacks():
+    shape = synth.TINY_INT2
+    for m in range(3):
+        q, packed, scales = synth.expert_matrix(shape, 0, 0, "routed", 2, m)
+        rows, k = q.shape
+        assert packed.shape == (rows, k // 4)
+        assert np.array_equal(oracle.unpack_weight_rows(packed, rows, k, 2), q)
+        # all four codes of the container occur; the row maximum rounds to 2
+        # and is clamped to 1
+        assert sorted(np.unique(q).tolist()) == [-2, -1, 0, 1]
+        assert scales.dtype == np.float32 and np.all(scales > 0)
+    assert synth.GLM_INT2.record_bytes() == 3 * 6144 * 2048 // 4
+
+
 def test_record_layout_and_sizes():
     for shape in (synth.TINY,):
         rec, sc = synth.expert_record(shape, 0, 0, "routed", 0)
