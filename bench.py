@@ -437,6 +437,8 @@ def secondary(device, b):
     del xp, ws, idx, w, y
     res["glm_gs64_decode_b1"] = gs64_bench(device, b)
     res["glm_gs64_mtp_verify_t4"] = gs64_bench(device, b, calls=100, T=4)
+    res["glm_int2_decode_b1"] = gs64_bench(device, b, shape=synth.GLM_INT2)
+    res["glm_int2_mtp_verify_t4"] = gs64_bench(device, b, calls=100, T=4, shape=synth.GLM_INT2)
     res["glm_stack24_mtp1_b32"] = stack_bench(device, b)
     return res
 
@@ -551,14 +553,14 @@ def few_only(args):
                       "status": cm.coli_moe_status(ws)}), flush=True)
 
 
-def gs64_bench(device, b, calls=300, T=1):
-    """The decode workload on group-scaled int4 experts (one fp32 scale per 64
-    weights of a row): 8 rotated copies of the layer, one coli_moe_layer call
-    (one fused launch) per position."""
+def gs64_bench(device, b, calls=300, T=1, shape=synth.GLM_GS64):
+    """The decode workload on another weight format of the same layer --
+    group-scaled int4 (one fp32 scale per 64 weights of a row, the default) or
+    packed int2 with per-row scales: 8 rotated copies of the layer, one
+    coli_moe_layer call per call of T positions."""
     import torch
     import synth.gpu as sg
     cm = b.cm
-    shape = synth.GLM_GS64
     seed = synth.WORKLOADS["glm_decode_b1"][1]
     cfg = cm.Cfg.of(shape)
     recs, scs = sg.expert_records(shape, seed, 0, "routed", shape.n_experts, device)
@@ -594,24 +596,27 @@ def gs64_bench(device, b, calls=300, T=1):
     out = {"tokens_per_s": round(T * calls / (ms / 1e3), 1), "us_per_call": round(1e3 * ms / calls, 2),
            "gbs": round(byt / (ms / 1e3) / 1e9, 1), "experts_per_call": round(uniq / calls, 2),
            "status": cm.coli_moe_status(ws),
-           "note": ("group-scaled int4 (gs64), the fused single-position kernel" if T == 1 else
-                    "group-scaled int4 (gs64) at 4 positions per call, the general expert kernel") +
-                   "; 8 rotated copies"}
+           "note": (("packed int2, per-row scales, the general expert kernel" if shape.weight_bits == 2 else
+                     "group-scaled int4 (gs64), the fused single-position kernel" if T == 1 else
+                     "group-scaled int4 (gs64), the general expert kernel") +
+                    f", {T} position(s) per call; 8 rotated copies")}
     del reps, Ws, recs, scs, srec, ssc
     torch.cuda.empty_cache()
     return out
 
 
-def gs64_only(args):
-    """--only gs64: the group-scaled decode measurement alone (for profiling)."""
+def gs64_only(args, shape=synth.GLM_GS64, name="gs64", fmt="group-scaled int4"):
+    """--only gs64 / int2: one weight format's decode and MTP-verify
+    measurements alone (for profiling)."""
     import torch
 
     class _B:  # the two attributes gs64_bench reads
         import quantized_expert_ffn_sigmoid_gb300 as cm
         R = REPLICAS
     for T in (1, 4):
-        print(json.dumps({"workload": f"gs64: GLM-5.2-shaped layer, group-scaled int4, {T} position(s) per call",
-                          **gs64_bench(torch.device("cuda", 0), _B, calls=300 if T == 1 else 100, T=T)}),
+        print(json.dumps({"workload": f"{name}: GLM-5.2-shaped layer, {fmt}, {T} position(s) per call",
+                          **gs64_bench(torch.device("cuda", 0), _B, calls=300 if T == 1 else 100, T=T,
+                                       shape=shape)}),
               flush=True)
 
 
@@ -802,7 +807,7 @@ def main():
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--no-secondary", dest="secondary", action="store_false")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
-    ap.add_argument("--only", choices=["prefill", "mtp", "b32", "gs64"], default=None,
+    ap.add_argument("--only", choices=["prefill", "mtp", "b32", "gs64", "int2"], default=None,
                     help="time one secondary workload alone (profiling)")
     ap.add_argument("--calls", type=int, default=20, help="calls per step of --only mtp / b32")
     ap.add_argument("--prefill-experts", type=int, default=256)
@@ -821,6 +826,8 @@ def main():
         few_only(args)
     elif args.only == "gs64":
         gs64_only(args)
+    elif args.only == "int2":
+        gs64_only(args, shape=synth.GLM_INT2, name="int2", fmt="packed int2 with per-row scales")
     else:
         run_gpu(args)
 

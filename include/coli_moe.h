@@ -64,9 +64,13 @@ extern "C" {
  * n_shared > 0, n_experts <= 1024, n_experts % n_groups == 0,
  * n_groups <= 32, 1 <= topk_group <= n_groups,
  * 1 <= top_k <= topk_group * n_experts / n_groups, top_k <= 32,
- * 0 <= n_shared <= 8, weight_bits in {4, 8}; a gate+up row pair of hidden
- * and four down rows of max(inter, shared_inter) must each fit in 32 KiB
- * (int4: hidden <= 32768, intermediate sizes <= 16384; int8: half). */
+ * 0 <= n_shared <= 8, weight_bits in {2, 4, 8}; a gate+up row pair of
+ * hidden and four down rows of max(inter, shared_inter) must each fit in
+ * 32 KiB (int4: hidden <= 32768, intermediate sizes <= 16384; int8: half;
+ * int2: double).  Packed int2 (colibrì v1.0 README, "What's implemented":
+ * int8 / packed int4 / packed int2 weights with per-row scales) takes
+ * per-row scales only and runs on the general expert kernel at every call
+ * size. */
 typedef struct coli_moe_cfg {
     int32_t hidden;                 /* H                                    */
     int32_t n_experts;              /* E routed experts                     */
@@ -76,11 +80,12 @@ typedef struct coli_moe_cfg {
     int32_t inter;                  /* I, intermediate size of routed experts */
     int32_t n_shared;               /* always-on shared experts             */
     int32_t shared_inter;           /* intermediate size of shared experts  */
-    int32_t weight_bits;            /* 4: packed int4, 8: int8              */
+    int32_t weight_bits;            /* 4: packed int4, 2: packed int2, 8: int8 */
     float   routed_scaling_factor;  /* multiplies the renormalised weights  */
     int32_t group_size;             /* 0: one scale per output row;
                                        64: one per 64 weights of a row ("gs64",
-                                       int4 only: COLI_EUNSUPPORTED with int8) */
+                                       int4 only: COLI_EUNSUPPORTED with int8
+                                       or int2) */
 } coli_moe_cfg;
 
 /* Expert weights.  One expert "record" is its three matrices stored adjacent
@@ -92,6 +97,9 @@ typedef struct coli_moe_cfg {
  *   weight_bits 4: two codes per byte; byte j of a row holds element 2j in the
  *                  low nibble and 2j+1 in the high nibble, each stored as
  *                  code + 8 (codes in [-8, 7]).
+ *   weight_bits 2: four codes per byte; byte j of a row holds elements
+ *                  4j .. 4j+3, element 4j+m in bits 2m and 2m+1, each stored
+ *                  as code + 2 (codes in [-2, 1]).
  * Records are consecutive: expert e starts at experts + e * record_bytes,
  * record_bytes = (2*Ie*H + H*Ie) * weight_bits / 8.
  * Scales are fp32 per output row, consecutive per expert:
@@ -210,7 +218,9 @@ const char* coli_moe_strerror(int code);
  * with P = T*k + n_shared*T and Imax = max(inter, shared_inter).  For
  * weight_bits 4, qx and qh hold each group of 8 consecutive codes in the
  * order 0,2,4,6,1,3,5,7 (the order of the low then high nibbles of 4 packed
- * bytes); for weight_bits 8 the order is natural. */
+ * bytes); for weight_bits 2 each group of 16 in the order 0,4,8,12, 1,5,9,13,
+ * 2,6,10,14, 3,7,11,15 (the order of the four 2-bit fields of 4 packed bytes);
+ * for weight_bits 8 the order is natural. */
 typedef struct coli_moe_ws_layout {
     size_t status, n_entries, entry_expert, entry_count, entry_offset,
            pair_token, pair_slot_of, qx, dx, qh, dh, o, total;

@@ -45,7 +45,7 @@ int check_cfg(const coli_moe_cfg* c) {
   if (c->inter <= 0 || c->inter % 128) return COLI_EINVAL;
   if (c->n_shared < 0 || c->n_shared > MAX_SHARED) return COLI_EINVAL;
   if (c->n_shared > 0 && (c->shared_inter <= 0 || c->shared_inter % 128)) return COLI_EINVAL;
-  if (c->weight_bits != 4 && c->weight_bits != 8) return COLI_EINVAL;
+  if (c->weight_bits != 2 && c->weight_bits != 4 && c->weight_bits != 8) return COLI_EINVAL;
   if (c->group_size != 0 && c->group_size != 64) return COLI_EINVAL;
   if (c->group_size != 0 && c->weight_bits != 4) return COLI_EUNSUPPORTED;  // group scales: int4 only
   if (!(c->routed_scaling_factor == c->routed_scaling_factor)) return COLI_EINVAL;
@@ -57,10 +57,11 @@ int check_cfg(const coli_moe_cfg* c) {
   return COLI_OK;
 }
 
-// The few-position, small-batch and prefill paths take per-row scales;
-// group-scaled weights run on the single-position kernel (which takes both)
-// or else on the general expert kernel.
-bool per_row(const coli_moe_cfg& c) { return c.group_size == 0; }
+// The few-position, small-batch and prefill paths take int4 or int8 weights
+// with per-row scales; group-scaled int4 runs on the single-position kernel
+// (which takes both scale layouts) or else on the general expert kernel, and
+// packed int2 on the general expert kernel at every call size.
+bool fast_paths(const coli_moe_cfg& c) { return c.group_size == 0 && c.weight_bits != 2; }
 
 coli_moe_cfg normalized(const coli_moe_cfg* c) {
   coli_moe_cfg n = *c;
@@ -133,19 +134,19 @@ int do_experts(const coli_moe_cfg& c, const coli_moe_weights* w, int T, const fl
     if (n_sm <= 0) return COLI_ECUDA;
     return rc_of(launch_decode(P, x, idx, x == nullptr, n_sm, st, dump_gu || dump_d));
   }
-  if (per_row(c) && prefill_fits(c, T)) {
+  if (fast_paths(c) && prefill_fits(c, T)) {
     // many positions: the expert products on the tensor cores
     const int n_sm = sm_count();
     if (n_sm <= 0) return COLI_ECUDA;
     return rc_of(launch_prefill(P, T, n_sm, st, dump_gu || dump_d));
   }
-  if (T <= GEMV_MAX_T && per_row(c) && gemv_fits(c, L)) {
+  if (T <= GEMV_MAX_T && fast_paths(c) && gemv_fits(c, L)) {
     // a few positions: stream the weights through the two GEMV kernels
     const int n_sm = sm_count();
     if (n_sm <= 0) return COLI_ECUDA;
     return rc_of(launch_gemv(P, n_sm, st, dump_gu || dump_d));
   }
-  if (per_row(c) && sb_fits(c, L)) {
+  if (fast_paths(c) && sb_fits(c, L)) {
     // up to a few dozen positions: weight rows on lanes, K split over warps
     const int n_sm = sm_count();
     if (n_sm <= 0) return COLI_ECUDA;

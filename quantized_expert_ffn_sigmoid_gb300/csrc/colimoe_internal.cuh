@@ -34,7 +34,7 @@ constexpr int PF_MIN_T = 64;    // calls with at least this many positions take 
 
 constexpr uint32_t SPIN_LIMIT = 1u << 22;  // bounded waits (about a second or more)
 
-__host__ __device__ inline int row_bytes(int k, int bits) { return bits == 4 ? k / 2 : k; }
+__host__ __device__ inline int row_bytes(int k, int bits) { return bits == 4 ? k / 2 : bits == 2 ? k / 4 : k; }
 
 // K ranges of the tiled router GEMM (calls of more than ROUTE_GEMV_MAX_T
 // positions): about 1024 CTAs of 64 x 64 logits, at least 192 K elements
@@ -122,6 +122,15 @@ __host__ __device__ inline int perm8(int i) {
   int r = i & 7;
   return (i & ~7) | ((r & 1) << 2) | (r >> 1);
 }
+// The same for packed-int2 weights: within each 16 elements (one 32-bit
+// weight word) element 4j+m is stored at byte 4m+j, so that the m-th 2-bit
+// field of 4 packed bytes meets elements m, 4+m, 8+m, 12+m in one 32-bit word.
+__host__ __device__ inline int perm16(int i) { return (i & ~15) | ((i & 3) << 2) | ((i >> 2) & 3); }
+// Position of natural element i of an activation block for weights of `bits`
+// bits, and the offset-binary bias of those weight codes (the block sum of the
+// activation codes times this bias is subtracted from each unsigned block dot).
+__host__ __device__ inline int act_pos(int i, int bits) { return bits == 4 ? perm8(i) : bits == 2 ? perm16(i) : i; }
+__host__ __device__ inline int code_bias(int bits) { return bits == 4 ? 8 : bits == 2 ? 2 : 0; }
 
 // ---------------------------------------------------------------- params
 struct ExpertParams {

@@ -84,12 +84,12 @@ __global__ void __launch_bounds__(PREP_THREADS) prep_kernel(PrepParams P) {
       bool bad;
       int q = q8_0_lane(v, &dd, &bad);
       anybad |= bad;
-      int pos = BITS == 4 ? perm8(lane) : lane;
+      int pos = act_pos(lane, BITS);
       qx[b * QB + pos] = (int8_t)q;
       int sum = warp_sum_i(q);
       if (lane == 0) {
         dx[b] = dd;
-        xs[b] = BITS == 4 ? 8 * sum : 0;
+        xs[b] = code_bias(BITS) * sum;
       }
     }
     if (anybad && lane == 0) atomicOr(status, COLI_STATUS_NONFINITE);
@@ -257,11 +257,11 @@ __global__ void __launch_bounds__(256) prep_small_kernel(PrepParams P) {
       bool bad;
       const int q = q8_0_lane(v, &dd, &bad);
       anybad |= bad;
-      qx[(size_t)b * QB + (BITS == 4 ? perm8(lane) : lane)] = (int8_t)q;
+      qx[(size_t)b * QB + act_pos(lane, BITS)] = (int8_t)q;
       const int sum = warp_sum_i(q);
       if (lane == 0) {
         dx[b] = dd;
-        xs[b] = BITS == 4 ? 8 * sum : 0;
+        xs[b] = code_bias(BITS) * sum;
       }
     }
     if (anybad && lane == 0) atomicOr(status, COLI_STATUS_NONFINITE);
@@ -392,6 +392,10 @@ cudaError_t launch_prep(const PrepParams& P, unsigned grid, size_t smem, cudaStr
     e = cudaFuncSetAttribute(prep_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     prep_kernel<4><<<grid, PREP_THREADS, smem, st>>>(P);
+  } else if (P.cfg.weight_bits == 2) {
+    e = cudaFuncSetAttribute(prep_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    prep_kernel<2><<<grid, PREP_THREADS, smem, st>>>(P);
   } else {
     e = cudaFuncSetAttribute(prep_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
@@ -411,6 +415,7 @@ cudaError_t launch_prep_small(const PrepParams& P, unsigned grid, cudaStream_t s
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   if (P.cfg.weight_bits == 4) return cudaLaunchKernelEx(&cfg, prep_small_kernel<4>, P);
+  if (P.cfg.weight_bits == 2) return cudaLaunchKernelEx(&cfg, prep_small_kernel<2>, P);
   return cudaLaunchKernelEx(&cfg, prep_small_kernel<8>, P);
 }
 

@@ -1,7 +1,8 @@
 // The expert products of the routed-MoE layer as one persistent kernel.
 //
 // colibrì v1.0 README, "What's implemented": integer-dot kernels on Q8_0-style
-// int8 activations against int8 / packed int4 weights with per-row scales;
+// int8 activations against int8 / packed int4 / packed int2 weights with
+// per-row scales;
 // batch-union (each distinct expert read once for all positions routed to
 // it); the always-on shared expert.  "Experimental Metal backend": the
 // routed-expert SwiGLU.  The combine is the gate-weighted sum of the
@@ -86,10 +87,11 @@ __device__ __forceinline__ void unpack4(uint32_t w, uint32_t& lo, uint32_t& hi) 
   hi = (w >> 4) & 0x0F0F0F0Fu;
 }
 
-// Integer dot of one 32-block: weights (16 bytes int4 or 32 bytes int8 in
-// shared memory) against one activation block (32 bytes, layout matching).
-// For int4 the nibbles are unsigned (code + 8): the block sum of 8*q_x is
-// subtracted, giving the exact signed result.
+// Integer dot of one 32-block: weights (16 bytes int4, 8 bytes int2 or 32
+// bytes int8 in shared memory) against one activation block (32 bytes, layout
+// matching).  For int4 / int2 the stored codes are unsigned (code + 8 / code
+// + 2): the block sum of 8*q_x / 2*q_x is subtracted, giving the exact signed
+// result.
 template <int BITS>
 struct BlockW {
   uint32_t v[8];
@@ -98,6 +100,14 @@ struct BlockW {
       uint4 w = *reinterpret_cast<const uint4*>(p);
       unpack4(w.x, v[0], v[1]); unpack4(w.y, v[2], v[3]);
       unpack4(w.z, v[4], v[5]); unpack4(w.w, v[6], v[7]);
+    } else if (BITS == 2) {
+      // word m of each half block: the m-th 2-bit field of its 4 bytes
+      const uint2 w = *reinterpret_cast<const uint2*>(p);
+#pragma unroll
+      for (int m = 0; m < 4; ++m) {
+        v[m] = (w.x >> (2 * m)) & 0x03030303u;
+        v[4 + m] = (w.y >> (2 * m)) & 0x03030303u;
+      }
     } else {
       uint4 a = reinterpret_cast<const uint4*>(p)[0], b = reinterpret_cast<const uint4*>(p)[1];
       v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
@@ -106,7 +116,7 @@ struct BlockW {
   __device__ __forceinline__ int dot(const uint4& a0, const uint4& a1, int corr) const {
     // two independent dp4a chains (latency), joined at the end
     int s = 0, r = 0;
-    if (BITS == 4) {
+    if (BITS != 8) {
       s = dp4a_us(v[0], a0.x, s); r = dp4a_us(v[1], a0.y, r); s = dp4a_us(v[2], a0.z, s);
       r = dp4a_us(v[3], a0.w, r); s = dp4a_us(v[4], a1.x, s); r = dp4a_us(v[5], a1.y, r);
       s = dp4a_us(v[6], a1.z, s); r = dp4a_us(v[7], a1.w, r);
@@ -299,7 +309,7 @@ __device__ void consume_a(const ExpertParams& P, const SmemPtrs& S, const ItemDe
   const int8_t* qa = reinterpret_cast<const int8_t*>(A);
   const float* da = reinterpret_cast<const float*>(A + TG * H);
   const int* xa = reinterpret_cast<const int*>(A + TG * H + TG * nb * 4);
-  const int cbytes = BITS == 4 ? 16 : 32;
+  const int cbytes = QB * BITS / 8;
   uint32_t* status = reinterpret_cast<uint32_t*>(P.ws + P.L.status);
   const int nst = RA / rs;
   // group-scaled weights: the scale of (row, block cc) is gsc[row * ngr + cc / 2]
@@ -396,13 +406,13 @@ __device__ void finish_a(const ExpertParams& P, const SmemPtrs& S, const ItemDes
     const int q = q8_0_lane(h, &dd, &bad);
     const int qs = warp_sum_i(q);
     const int p = d.pair0 + t;
-    const int pos = BITS == 4 ? perm8(r) : r;
+    const int pos = act_pos(r, BITS);
     int8_t* qh = reinterpret_cast<int8_t*>(ws + L.qh);
     qh[(size_t)p * L.imax + d.tile * RA + pos] = (int8_t)q;
     if (lane == 0) {
       const int nbI = L.imax / QB;
       reinterpret_cast<float*>(ws + L.dh)[(size_t)p * nbI + d.tile] = dd;
-      reinterpret_cast<int32_t*>(ws + L.hs)[(size_t)p * nbI + d.tile] = BITS == 4 ? 8 * qs : 0;
+      reinterpret_cast<int32_t*>(ws + L.hs)[(size_t)p * nbI + d.tile] = code_bias(BITS) * qs;
       if (bad) atomicOr(status, COLI_STATUS_NONFINITE);
     }
   }
@@ -429,7 +439,7 @@ __device__ void consume_b(const ExpertParams& P, const SmemPtrs& S, const ItemDe
   const int8_t* qa = reinterpret_cast<const int8_t*>(A);
   const float* da = reinterpret_cast<const float*>(A + TG * im);
   const int* xa = reinterpret_cast<const int*>(A + TG * im + TG * nbI * 4);
-  const int cbytes = BITS == 4 ? 16 : 32;
+  const int cbytes = QB * BITS / 8;
   uint32_t* status = reinterpret_cast<uint32_t*>(P.ws + L.status);
   const int H = P.cfg.hidden;
   const int nst = RB / rs;
@@ -617,6 +627,8 @@ static cudaError_t launch_one(const ExpertParams& P, int grid, size_t smem, cuda
 cudaError_t launch_experts(const ExpertParams& P, int grid, size_t smem, cudaStream_t st, bool dump) {
   if (P.cfg.weight_bits == 4)
     return dump ? launch_one<4, true>(P, grid, smem, st) : launch_one<4, false>(P, grid, smem, st);
+  if (P.cfg.weight_bits == 2)
+    return dump ? launch_one<2, true>(P, grid, smem, st) : launch_one<2, false>(P, grid, smem, st);
   return dump ? launch_one<8, true>(P, grid, smem, st) : launch_one<8, false>(P, grid, smem, st);
 }
 

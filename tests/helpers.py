@@ -47,3 +47,12 @@ def unpermute_int4(q):
     out[..., 0::2] = g[..., 0:4]
     out[..., 1::2] = g[..., 4:8]
     return out.reshape(q.shape)
+
+
+def unpermute_int2(q):
+    """Undo the library's in-block order for packed-int2 layouts: within each
+    16 codes, natural element 4j+m is stored at position 4m+j."""
+    q = np.asarray(q)
+    g = q.reshape(*q.shape[:-1], q.shape[-1] // 16, 16)
+    src = [4 * (i % 4) + i // 4 for i in range(16)]
+    return g[..., src].reshape(q.shape)

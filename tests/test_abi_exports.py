@@ -80,3 +80,17 @@ def test_group_size_host_checks(lib):
                 dataclasses.replace(synth.GLM_GS64, weight_bits=8)):
         assert cm.coli_moe_workspace_size(cm.Cfg.of(bad), 4) == 0
     assert cm.Cfg.of(synth.GLM).group_size == 0
+
+
+def test_weight_bits_host_checks(lib):
+    # 2, 4 or 8 bits; group scales only with int4 (not with packed int2)
+    import dataclasses
+    import synth
+    import quantized_expert_ffn_sigmoid_gb300 as cm
+    n4 = cm.coli_moe_workspace_size(cm.Cfg.of(synth.GLM), 4)
+    assert cm.coli_moe_workspace_size(cm.Cfg.of(synth.GLM_INT2), 4) == n4 > 0
+    assert cm.coli_moe_workspace_size(cm.Cfg.of(synth.TINY_INT2), 4) > 0
+    for bad in (dataclasses.replace(synth.GLM_INT2, group_size=64),
+                dataclasses.replace(synth.GLM, weight_bits=3),
+                dataclasses.replace(synth.GLM, weight_bits=1)):
+        assert cm.coli_moe_workspace_size(cm.Cfg.of(bad), 4) == 0
