@@ -69,8 +69,8 @@ extern "C" {
  * 32 KiB (int4: hidden <= 32768, intermediate sizes <= 16384; int8: half;
  * int2: double).  Packed int2 (colibrì v1.0 README, "What's implemented":
  * int8 / packed int4 / packed int2 weights with per-row scales) takes
- * per-row scales only and runs on the general expert kernel at every call
- * size. */
+ * per-row scales only; it runs on the fused single-position kernel for one
+ * position per call and on the general expert kernel otherwise. */
 typedef struct coli_moe_cfg {
     int32_t hidden;                 /* H                                    */
     int32_t n_experts;              /* E routed experts                     */

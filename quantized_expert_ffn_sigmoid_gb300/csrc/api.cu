@@ -60,7 +60,7 @@ int check_cfg(const coli_moe_cfg* c) {
 // The few-position, small-batch and prefill paths take int4 or int8 weights
 // with per-row scales; group-scaled int4 runs on the single-position kernel
 // (which takes both scale layouts) or else on the general expert kernel, and
-// packed int2 on the general expert kernel at every call size.
+// packed int2 likewise on the single-position kernel or the general one.
 bool fast_paths(const coli_moe_cfg& c) { return c.group_size == 0 && c.weight_bits != 2; }
 
 coli_moe_cfg normalized(const coli_moe_cfg* c) {

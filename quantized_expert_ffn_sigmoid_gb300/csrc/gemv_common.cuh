@@ -50,6 +50,22 @@ template <> struct WBlk<8> {
   }
 };
 
+template <> struct WBlk<2> {
+  uint2 w;  // 32 two-bit fields
+  __device__ __forceinline__ void lds(const uint8_t* p) { w = *reinterpret_cast<const uint2*>(p); }
+  __device__ __forceinline__ int dot(const uint4& a0, const uint4& a1, int corr) const {
+    // field m of every byte masked in place: its products come out times 4^m,
+    // and one exact shift per chain undoes it (activation word m of each half
+    // block holds the elements that field m of the 4 weight bytes carries)
+    int c0 = 0, c1 = 0, c2 = 0, c3 = 0;
+    c0 = dp4a_us(w.x & 0x03030303u, a0.x, c0); c1 = dp4a_us(w.x & 0x0C0C0C0Cu, a0.y, c1);
+    c2 = dp4a_us(w.x & 0x30303030u, a0.z, c2); c3 = dp4a_us(w.x & 0xC0C0C0C0u, a0.w, c3);
+    c0 = dp4a_us(w.y & 0x03030303u, a1.x, c0); c1 = dp4a_us(w.y & 0x0C0C0C0Cu, a1.y, c1);
+    c2 = dp4a_us(w.y & 0x30303030u, a1.z, c2); c3 = dp4a_us(w.y & 0xC0C0C0C0u, a1.w, c3);
+    return (c0 + (c1 >> 2) + (c2 >> 4) + (c3 >> 6)) - corr;  // fields hold code + 2: remove 2 * sum(q_x)
+  }
+};
+
 __device__ __forceinline__ const uint8_t* gemv_record(const ExpertParams& P, int expert, int* inter,
                                                       const float** sc) {
   const coli_moe_cfg& c = P.cfg;

@@ -1,7 +1,8 @@
 """GPU parity of packed int2 weights (four codes per byte, per-row fp32
 scales) against the CPU oracle, through the C ABI: routing, tables, Q8_0
 codes and int32 block dots bit-exact, requantised h exact where unique,
-outputs within 1e-3."""
+outputs within 1e-3.  One position per call runs the fused single-position
+kernel, more positions the general expert kernel."""
 import numpy as np
 import pytest
 
@@ -97,10 +98,12 @@ def test_glm_int2_parity(glm2, T):
     print("int2 T", T, st)
 
 
-def test_glm_int2_layer_call(glm2):
-    """coli_moe_layer (router, dispatch, experts) on packed int2 experts."""
+def test_glm_int2_fused_decode(glm2):
+    """One fused launch per position (router inside) on packed int2 experts,
+    two calls in a row on one workspace; the split calls give the same y."""
     ws = cm.new_workspace(glm2.cfg, 1)
-    x, _, _ = margin_batch(glm2.shape, glm2.seed, "glm_int2_layer", 1, glm2.router_w, glm2.bias)
-    g = glm2.run(x, layer=True, ws=ws)
-    check_parity(glm2, x, g)
-    assert np.array_equal(g["y"], glm2.run(x, dump=False, ws=ws)["y"])
+    for p in range(2):
+        x, _, _ = margin_batch(glm2.shape, glm2.seed, "glm_int2_layer", 1, glm2.router_w, glm2.bias, start=p)
+        g = glm2.run(x, layer=True, ws=ws)
+        check_parity(glm2, x, g)
+        assert np.array_equal(g["y"], glm2.run(x, dump=False, ws=ws)["y"])
