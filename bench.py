@@ -597,7 +597,9 @@ def gs64_bench(device, b, calls=300, T=1, shape=synth.GLM_GS64):
            "gbs": round(byt / (ms / 1e3) / 1e9, 1), "experts_per_call": round(uniq / calls, 2),
            "status": cm.coli_moe_status(ws),
            "note": (("packed int2, per-row scales" if shape.weight_bits == 2 else "group-scaled int4 (gs64)") +
-                    (", the fused single-position kernel" if T == 1 else ", the general expert kernel") +
+                    (", the fused single-position kernel" if T == 1 else
+                     ", the few-position kernels" if shape.weight_bits == 2 and T <= 4 else
+                     ", the general expert kernel") +
                     f", {T} position(s) per call; 8 rotated copies")}
     del reps, Ws, recs, scs, srec, ssc
     torch.cuda.empty_cache()

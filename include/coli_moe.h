@@ -70,7 +70,8 @@ extern "C" {
  * int2: double).  Packed int2 (colibrì v1.0 README, "What's implemented":
  * int8 / packed int4 / packed int2 weights with per-row scales) takes
  * per-row scales only; it runs on the fused single-position kernel for one
- * position per call and on the general expert kernel otherwise. */
+ * position per call, on the few-position kernels for 2 to 4 and on the
+ * general expert kernel beyond. */
 typedef struct coli_moe_cfg {
     int32_t hidden;                 /* H                                    */
     int32_t n_experts;              /* E routed experts                     */

@@ -57,11 +57,13 @@ int check_cfg(const coli_moe_cfg* c) {
   return COLI_OK;
 }
 
-// The few-position, small-batch and prefill paths take int4 or int8 weights
-// with per-row scales; group-scaled int4 runs on the single-position kernel
-// (which takes both scale layouts) or else on the general expert kernel, and
-// packed int2 likewise on the single-position kernel or the general one.
-bool fast_paths(const coli_moe_cfg& c) { return c.group_size == 0 && c.weight_bits != 2; }
+// The few-position path takes per-row scales (int8, int4 or int2); the
+// small-batch and prefill paths take int4 or int8 with per-row scales.
+// Group-scaled int4 runs on the single-position kernel (which takes both
+// scale layouts) or else on the general expert kernel, and packed int2
+// beyond the few-position sizes on the general expert kernel.
+bool per_row(const coli_moe_cfg& c) { return c.group_size == 0; }
+bool fast_paths(const coli_moe_cfg& c) { return per_row(c) && c.weight_bits != 2; }
 
 coli_moe_cfg normalized(const coli_moe_cfg* c) {
   coli_moe_cfg n = *c;
@@ -140,7 +142,7 @@ int do_experts(const coli_moe_cfg& c, const coli_moe_weights* w, int T, const fl
     if (n_sm <= 0) return COLI_ECUDA;
     return rc_of(launch_prefill(P, T, n_sm, st, dump_gu || dump_d));
   }
-  if (T <= GEMV_MAX_T && fast_paths(c) && gemv_fits(c, L)) {
+  if (T <= GEMV_MAX_T && per_row(c) && gemv_fits(c, L)) {
     // a few positions: stream the weights through the two GEMV kernels
     const int n_sm = sm_count();
     if (n_sm <= 0) return COLI_ECUDA;

@@ -44,7 +44,7 @@ struct GuItem { int tile, ntok, pair0, inter; const uint8_t* rec; const float* s
 // activation blocks of the single position then live in registers).
 template <int BITS, int NT, bool DUMP>
 __global__ void __launch_bounds__(GU_THREADS, 1) gemv_gu_kernel(ExpertParams P) {
-  constexpr int CBYTES = BITS == 4 ? 16 : 32;
+  constexpr int CBYTES = QB * BITS / 8;  // bytes of one 32-block of a weight row
   constexpr int RCPL = 8;  // register-resident blocks per lane when NT == 1
   const coli_moe_cfg& c = P.cfg;
   const Layout& L = P.L;
@@ -307,12 +307,12 @@ __global__ void __launch_bounds__(GU_THREADS, 1) gemv_gu_kernel(ExpertParams P) 
       const int qv = q8_0_lane(hbuf[lane * TG + t], &dd, &bad);
       const int qs = warp_sum_i(qv);
       const int p = d.pair0 + t;
-      const int pos = BITS == 4 ? perm8(lane) : lane;
+      const int pos = act_pos(lane, BITS);
       reinterpret_cast<int8_t*>(ws + L.qh)[(size_t)p * L.imax + d.tile * RA + pos] = (int8_t)qv;
       if (lane == 0) {
         const int nbI = L.imax / QB;
         reinterpret_cast<float*>(ws + L.dh)[(size_t)p * nbI + d.tile] = dd;
-        reinterpret_cast<int32_t*>(ws + L.hs)[(size_t)p * nbI + d.tile] = BITS == 4 ? 8 * qs : 0;
+        reinterpret_cast<int32_t*>(ws + L.hs)[(size_t)p * nbI + d.tile] = code_bias(BITS) * qs;
         if (bad) atomicOr(status, COLI_STATUS_NONFINITE);
       }
     }
@@ -366,7 +366,7 @@ __host__ __device__ inline DnGeo dn_geo(const coli_moe_cfg& c, const Layout& L, 
 
 template <int BITS, int MT, bool DUMP>
 __global__ void __launch_bounds__(DN_MAX_NW * 32, 1) gemv_down_kernel(ExpertParams P, int nslot) {
-  constexpr int CBYTES = BITS == 4 ? 16 : 32;
+  constexpr int CBYTES = QB * BITS / 8;  // bytes of one 32-block of a weight row
   const coli_moe_cfg& c = P.cfg;
   const Layout& L = P.L;
   uint8_t* ws = P.ws;
@@ -639,6 +639,8 @@ static cudaError_t launch_gemv_t(const ExpertParams& P, int n_sm, cudaStream_t s
 cudaError_t launch_gemv(const ExpertParams& P, int n_sm, cudaStream_t st, bool dump) {
   if (P.cfg.weight_bits == 4)
     return dump ? launch_gemv_t<4, true>(P, n_sm, st) : launch_gemv_t<4, false>(P, n_sm, st);
+  if (P.cfg.weight_bits == 2)
+    return dump ? launch_gemv_t<2, true>(P, n_sm, st) : launch_gemv_t<2, false>(P, n_sm, st);
   return dump ? launch_gemv_t<8, true>(P, n_sm, st) : launch_gemv_t<8, false>(P, n_sm, st);
 }
 

@@ -2,7 +2,8 @@
 scales) against the CPU oracle, through the C ABI: routing, tables, Q8_0
 codes and int32 block dots bit-exact, requantised h exact where unique,
 outputs within 1e-3.  One position per call runs the fused single-position
-kernel, more positions the general expert kernel."""
+kernel, two to four the few-position (GEMV) kernels, more the general expert
+kernel."""
 import numpy as np
 import pytest
 
@@ -35,7 +36,7 @@ def tiny2():
     return DeviceLayer(synth.TINY_INT2, 10)
 
 
-@pytest.mark.parametrize("T", [1, 2, 4, 5, 8, 13, 33, 70])
+@pytest.mark.parametrize("T", [1, 2, 3, 4, 5, 8, 13, 33, 70])
 def test_tiny_int2_parity(tiny2, T):
     x, _, _ = margin_batch(tiny2.shape, tiny2.seed, ("int2", T), T, tiny2.router_w, tiny2.bias)
     check_parity(tiny2, x, tiny2.run(x))
@@ -51,14 +52,17 @@ def test_tiny_int2_layer_call(tiny2, T):
 
 
 def test_int2_given_routing_edge_cases(tiny2):
-    """Duplicate ids, skipped slots and an all-skipped position, at several
-    positions per call and at one."""
+    """Duplicate ids, skipped slots and an all-skipped position, at five
+    positions per call (general kernel), four (few-position kernels) and one
+    (single-position kernel)."""
     x = synth.token_batch(tiny2.shape, 19, 0, range(5))
     idx = np.array([[0, 3, 3, 7], [15, -1, 2, -1], [1, 2, 5, 6], [-1, -1, -1, -1], [4, 4, 4, 4]])
     w = np.array([[0.5, 0.25, 0.25, 0.0], [1.0, 9.0, 0.0, 9.0], [1.0, 0.0, 0.0, 0.0],
                   [0.0, 0.0, 0.0, 0.0], [0.1, 0.2, 0.3, 0.4]], np.float32)
     g = tiny2.run(x, route=False, idx=idx, w=w)
     check_parity(tiny2, x, g, idx=idx, w=w.astype(np.float64))
+    g4 = tiny2.run(x[:4], route=False, idx=idx[:4], w=w[:4])
+    check_parity(tiny2, x[:4], g4, idx=idx[:4], w=w[:4].astype(np.float64))
     for p in (0, 3, 4):
         g1 = tiny2.run(x[p:p + 1], route=False, idx=idx[p:p + 1], w=w[p:p + 1])
         check_parity(tiny2, x[p:p + 1], g1, idx=idx[p:p + 1], w=w[p:p + 1].astype(np.float64))
