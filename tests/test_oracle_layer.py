@@ -90,3 +90,26 @@ def test_layer_matches_fp64_dequantised_path(tiny_layer):
         rec, sc = L["get_record"]("shared", 0)
         y[t] += oracle.expert_ffn_dequant_fp64(rec, sc, shape.hidden, shape.shared_inter, 4, x[t:t + 1])[0]
     assert np.allclose(out["y"], y, rtol=1e-9, atol=1e-12 * np.abs(y).max())
+
+
+def test_int2_layer_combine_and_dequantised_path():
+    """Packed int2 experts: the layer equals the dense every-expert evaluation
+    with a dense gate matrix, and the fp64 dequantised products."""
+    shape, seed = synth.TINY_INT2, 3
+    routed = [synth.expert_record(shape, seed, 0, "routed", e) for e in range(shape.n_experts)]
+    shared = [synth.expert_record(shape, seed, 0, "shared", 0)]
+    get = lambda kind, e: routed[e] if kind == "routed" else shared[e]
+    wr, bias = synth.router_weight(shape, seed), synth.router_bias(shape, seed)
+    x = synth.token_batch(shape, seed, 0, range(6))
+    out = oracle.moe_layer(shape, get, x, wr, bias)
+    dense = oracle.dense_reference(shape, get, x, _dense_gates(out["idx"], out["w"], shape.n_experts))
+    assert np.allclose(out["y"], dense, rtol=1e-12, atol=1e-14 * np.abs(dense).max())
+    y = np.zeros_like(out["y"])
+    for t in range(x.shape[0]):
+        for j in range(shape.top_k):
+            rec, sc = get("routed", int(out["idx"][t, j]))
+            y[t] += out["w"][t, j] * oracle.expert_ffn_dequant_fp64(
+                rec, sc, shape.hidden, shape.inter, 2, x[t:t + 1])[0]
+        rec, sc = get("shared", 0)
+        y[t] += oracle.expert_ffn_dequant_fp64(rec, sc, shape.hidden, shape.shared_inter, 2, x[t:t + 1])[0]
+    assert np.allclose(out["y"], y, rtol=1e-9, atol=1e-12 * np.abs(y).max())
