@@ -435,10 +435,10 @@ def secondary(device, b):
                                              "on this GPU, which has no tcgen05 int8 MMA; bf16: " + kind +
                                              " dense bf16, the rate of the kind::f16 MMA the kernel uses"}
     del xp, ws, idx, w, y
-    res["glm_gs64_decode_b1"] = gs64_bench(device, b)
-    res["glm_gs64_mtp_verify_t4"] = gs64_bench(device, b, calls=100, T=4)
-    res["glm_int2_decode_b1"] = gs64_bench(device, b, shape=synth.GLM_INT2)
-    res["glm_int2_mtp_verify_t4"] = gs64_bench(device, b, calls=100, T=4, shape=synth.GLM_INT2)
+    res["glm_gs64_decode_b1"] = weight_format_bench(device, b)
+    res["glm_gs64_mtp_verify_t4"] = weight_format_bench(device, b, calls=100, T=4)
+    res["glm_int2_decode_b1"] = weight_format_bench(device, b, shape=synth.GLM_INT2)
+    res["glm_int2_mtp_verify_t4"] = weight_format_bench(device, b, calls=100, T=4, shape=synth.GLM_INT2)
     res["glm_stack24_mtp1_b32"] = stack_bench(device, b)
     return res
 
@@ -553,7 +553,7 @@ def few_only(args):
                       "status": cm.coli_moe_status(ws)}), flush=True)
 
 
-def gs64_bench(device, b, calls=300, T=1, shape=synth.GLM_GS64):
+def weight_format_bench(device, b, calls=300, T=1, shape=synth.GLM_GS64):
     """The decode workload on another weight format of the same layer --
     group-scaled int4 (one fp32 scale per 64 weights of a row, the default) or
     packed int2 with per-row scales: 8 rotated copies of the layer, one
@@ -606,17 +606,17 @@ def gs64_bench(device, b, calls=300, T=1, shape=synth.GLM_GS64):
     return out
 
 
-def gs64_only(args, shape=synth.GLM_GS64, name="gs64", fmt="group-scaled int4"):
+def weight_format_only(args, shape=synth.GLM_GS64, name="gs64", fmt="group-scaled int4"):
     """--only gs64 / int2: one weight format's decode and MTP-verify
     measurements alone (for profiling)."""
     import torch
 
-    class _B:  # the two attributes gs64_bench reads
+    class _B:  # the two attributes weight_format_bench reads
         import quantized_expert_ffn_sigmoid_gb300 as cm
         R = REPLICAS
     for T in (1, 4):
         print(json.dumps({"workload": f"{name}: GLM-5.2-shaped layer, {fmt}, {T} position(s) per call",
-                          **gs64_bench(torch.device("cuda", 0), _B, calls=300 if T == 1 else 100, T=T,
+                          **weight_format_bench(torch.device("cuda", 0), _B, calls=300 if T == 1 else 100, T=T,
                                        shape=shape)}),
               flush=True)
 
@@ -826,9 +826,9 @@ def main():
     elif args.only in ("mtp", "b32"):
         few_only(args)
     elif args.only == "gs64":
-        gs64_only(args)
+        weight_format_only(args)
     elif args.only == "int2":
-        gs64_only(args, shape=synth.GLM_INT2, name="int2", fmt="packed int2 with per-row scales")
+        weight_format_only(args, shape=synth.GLM_INT2, name="int2", fmt="packed int2 with per-row scales")
     else:
         run_gpu(args)
 
