@@ -22,7 +22,8 @@ It computes the layer literally, following the colibrì pages:
 
 Floating point is fp64 except where a floating-point value decides an
 integer code (the Q8_0 scale and rounding), which is done in fp32 exactly as
-the kernel does it.  Integer block dot products are exact (int64).
+the kernel does it.  Integer block dot products are exact (fp64 products of
+8-bit codes are exact integers; returned as int64).
 
 Readings of points the pages leave open are listed in the docstrings of the
 functions that take them.  Parity status: every function here is pinned by

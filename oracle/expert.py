@@ -40,16 +40,24 @@ def block_dots(wq: np.ndarray, qx: np.ndarray) -> np.ndarray:
     """Exact per-32-block integer dot products.
 
     ``wq`` [R,K] weight codes, ``qx`` [T,K] activation codes ->
-    int64 [T,R,K/32].  Checks that every result fits int32."""
+    int64 [T,R,K/32].  Checks that every result fits int32.
+
+    Each block is one library matrix product in fp64.  The codes are 8-bit
+    integers, so every product and every partial sum of 32 of them is an
+    integer below 2**21 in magnitude and is represented exactly: the fp64
+    product IS the integer dot product, in any summation order."""
     wq = np.asarray(wq)
     qx = np.atleast_2d(np.asarray(qx))
     R, K = wq.shape
     if K % QBLOCK or qx.shape[1] != K:
         raise ValueError("shape mismatch")
+    if wq.dtype.itemsize > 1 or qx.dtype.itemsize > 1:
+        if (np.abs(wq).max(initial=0) > 255) or (np.abs(qx).max(initial=0) > 255):
+            raise ValueError("block dots take 8-bit codes")
     nb = K // QBLOCK
-    W = wq.reshape(R, nb, QBLOCK).astype(np.int64)
-    X = qx.reshape(qx.shape[0], nb, QBLOCK).astype(np.int64)
-    acc = np.einsum("rbk,tbk->trb", W, X)
+    W = wq.reshape(R, nb, QBLOCK).astype(np.float64).transpose(1, 2, 0)            # [nb, 32, R]
+    X = np.ascontiguousarray(qx.reshape(qx.shape[0], nb, QBLOCK).astype(np.float64).transpose(1, 0, 2))
+    acc = np.matmul(X, W).transpose(1, 2, 0).astype(np.int64)                          # [T, R, nb]
     if acc.size and (acc.max() > 2**31 - 1 or acc.min() < -2**31):
         raise OverflowError("block dot exceeds int32")
     return acc

@@ -29,6 +29,22 @@ def test_block_dot_brute_force():
                 assert acc[t, r, b] == ref
 
 
+def test_block_dot_full_int8_range_brute_force():
+    # int8 weights and codes at the extremes of their range, a GLM-5.2-sized
+    # reduction: sampled blocks against Python integer arithmetic
+    rng = np.random.default_rng(11)
+    w = rng.choice(np.array([-128, -127, -1, 0, 1, 126, 127], np.int8), (7, 6144))
+    x = rng.integers(-127, 128, (4, 6144)).astype(np.int8)
+    x[0] = -127
+    w[0] = -128
+    acc = oracle.block_dots(w, x)
+    assert acc.dtype == np.int64 and acc.shape == (4, 7, 192)
+    assert acc[0, 0, 0] == 32 * 128 * 127
+    for t, r, b in [(0, 0, 191), (1, 3, 0), (2, 6, 77), (3, 1, 150), (3, 6, 191)]:
+        ref = sum(int(w[r, 32 * b + i]) * int(x[t, 32 * b + i]) for i in range(32))
+        assert acc[t, r, b] == ref
+
+
 def _record(gate, up, down, bits=4):
     pk = {4: oracle.int4_pack, 2: oracle.int2_pack,
           8: lambda q: q.astype(np.int8).view(np.uint8)}[bits]
