@@ -255,13 +255,22 @@ int coli_moe_forward_dump(const coli_moe_cfg* cfg, const coli_moe_weights* weigh
  *     COLI_STATIC_WS_BYTES (24 MiB: the GLM-5.2-shaped layer up to T = 88);
  *     larger T returns COLI_EWORKSPACE and enqueues nothing.
  *   - The first call on a device looks up the array's device address
- *     (cudaGetSymbolAddress, with that device current) and caches it; make
- *     that first call before any stream capture.
+ *     (cudaGetSymbolAddress, with that device current) and caches it per
+ *     device ordinal for the life of the process; make that first call before
+ *     any stream capture.  The cache assumes the runtime's primary context:
+ *     after cudaDeviceReset, or from another driver-API context on the same
+ *     device, the cached address is stale and must not be used (this entry
+ *     point then gives undefined results).
  *   - Every call on a device shares the one array: calls that overlap on the
  *     GPU (different streams, or host threads without ordering) race and give
  *     wrong results.  Calls ordered on one stream are safe; each call rewrites
  *     every table and counter it reads.
- *   - Device status bits (non-finite input, bad ids) are not reported. */
+ *   - Device status bits (non-finite input, expert ids outside [-1, E), an
+ *     expired bounded wait) are recorded in the array but cannot be read or
+ *     cleared by the caller.  In those cases y is undefined: rows of
+ *     positions with non-finite x, or with an out-of-range id, and every row
+ *     after an expired wait may hold anything.  Callers that need to detect
+ *     them use coli_moe_forward with a workspace and coli_moe_status. */
 #define COLI_STATIC_WS_BYTES (24u << 20)
 int coli_moe_forward_static(const coli_moe_cfg* cfg, const coli_moe_weights* weights,
                             const float* x, int32_t T,

@@ -65,13 +65,21 @@ def union_tables(idx: np.ndarray, n_experts: int, n_shared: int):
 
 
 def moe_forward(shape, get_record, x: np.ndarray, idx: np.ndarray, w: np.ndarray,
-                keep_pairs: bool = False):
+                keep_pairs: bool = False, on_entry=None, map_fn=map, max_tokens: int | None = None):
     """Layer output for given routing (``idx`` [T,k], ``w`` [T,k]).
 
     ``get_record(kind, e)`` returns ``(record bytes, scales)`` for
     kind 'routed' or 'shared'.  Returns dict(y fp64 [T,H], y_err, qx, dx,
     pairs) where ``pairs[(kind, e)]`` holds the expert dict of ``expert_ffn``
-    for the tokens routed to it (if ``keep_pairs``)."""
+    for the tokens routed to it (if ``keep_pairs``).
+
+    Evaluation order only (each token's result is independent of the
+    others, as the batch-union description says): ``max_tokens`` splits an
+    expert's tokens into runs of at most that many, ``map_fn`` evaluates the
+    (expert, run) jobs (e.g. a thread pool's ``map``; results are combined in
+    job order, so the output does not depend on it), and ``on_entry(kind, e,
+    out)`` is called with each run's ``expert_ffn`` dict (plus ``tokens`` and
+    ``js``, the pairs' (t, j)) before its intermediates are dropped."""
     H = shape.hidden
     x = np.atleast_2d(np.asarray(x, np.float32))
     T = x.shape[0]
@@ -82,28 +90,46 @@ def moe_forward(shape, get_record, x: np.ndarray, idx: np.ndarray, w: np.ndarray
     yerr = np.zeros((T, H), np.float64)
     pairs = {}
     tabs = union_tables(idx, shape.n_experts, shape.n_shared)
-    for ui, e in enumerate(tabs["uniq"]):
+    group = getattr(shape, "group_size", 0)
+    run_len = max_tokens or max(T, 1)
+    jobs = []
+    for e in tabs["uniq"]:
         sel = np.argwhere(idx == e)              # (t, j) ascending
-        toks = sel[:, 0]
-        rec, sc = get_record("routed", int(e))
-        out = expert_ffn(rec, sc, H, shape.inter, shape.weight_bits, qx[toks], dx[toks],
-                         getattr(shape, "group_size", 0))
-        for n, (t, j) in enumerate(sel):
-            y[t] += w[t, j] * out["o"][n]
-            yerr[t] += abs(w[t, j]) * (out["o_err"][n] + np.abs(out["o"][n]) * 4 * U32)
-        if keep_pairs:
-            out["tokens"] = toks
-            out["js"] = sel[:, 1]
-            pairs[("routed", int(e))] = out
+        for c in range(0, len(sel), run_len):
+            jobs.append(("routed", int(e), sel[c:c + run_len]))
     for s in range(shape.n_shared):
-        rec, sc = get_record("shared", s)
-        out = expert_ffn(rec, sc, H, shape.shared_inter, shape.weight_bits, qx, dx,
-                         getattr(shape, "group_size", 0))
-        y += out["o"]
-        yerr += out["o_err"]
+        sel = np.stack([np.arange(T), np.full(T, -1)], axis=1)
+        for c in range(0, T, run_len):
+            jobs.append(("shared", s, sel[c:c + run_len]))
+
+    def run(job):
+        kind, e, sel = job
+        toks = sel[:, 0]
+        rec, sc = get_record(kind, e)
+        inter = shape.inter if kind == "routed" else shape.shared_inter
+        out = expert_ffn(rec, sc, H, inter, shape.weight_bits, qx[toks], dx[toks], group)
+        out["tokens"] = toks
+        out["js"] = sel[:, 1]
+        if on_entry is not None:
+            on_entry(kind, e, out)
+        return out if keep_pairs else dict(o=out["o"], o_err=out["o_err"])
+
+    for (kind, e, sel), out in zip(jobs, map_fn(run, jobs)):
+        for n, (t, j) in enumerate(sel):
+            if kind == "routed":
+                y[t] += w[t, j] * out["o"][n]
+                yerr[t] += abs(w[t, j]) * (out["o_err"][n] + np.abs(out["o"][n]) * 4 * U32)
+            else:
+                y[t] += out["o"][n]
+                yerr[t] += out["o_err"][n]
         if keep_pairs:
-            out["tokens"] = np.arange(T)
-            pairs[("shared", s)] = out
+            key = (kind, e)
+            if key in pairs:   # a later run of the same expert: append its pairs
+                prev = pairs[key]
+                pairs[key] = {k: (np.concatenate([prev[k], v]) if isinstance(v, np.ndarray) and v.ndim
+                                  else v) for k, v in out.items()}
+            else:
+                pairs[key] = out
     return dict(y=y, y_err=yerr, qx=qx, dx=dx, pairs=pairs, tables=tabs)
 
 

@@ -3,13 +3,17 @@ the library through its C ABI and compares every observable with the oracle.
 Imported only by tests marked ``gpu``."""
 from __future__ import annotations
 
+import concurrent.futures as cf
+import os
+import threading
+
 import numpy as np
 import torch
 
 import oracle
 import synth
 import quantized_expert_ffn_sigmoid_gb300 as cm
-from helpers import normwise_err, unpermute_int2, unpermute_int4
+from helpers import elementwise_err, normwise_err, unpermute_int2, unpermute_int4
 
 Y_TOL = 1e-3     # max normwise relative error of the layer output
 W_RTOL = 1e-5    # gate weights: fp32 router vs fp64 oracle
@@ -117,11 +121,22 @@ class DeviceLayer:
         return out
 
 
-def check_parity(layer: DeviceLayer, x, g, ref=None, idx=None, w=None, tokens=None):
+def _pool_size():
+    return max(1, min(16, os.cpu_count() or 1))
+
+
+def check_parity(layer: DeviceLayer, x, g, ref=None, idx=None, w=None, tokens=None, threads=None,
+                 max_tokens=32):
     """Compare GPU observables ``g`` with the oracle.  ``tokens`` restricts the
-    expert-level comparisons (and y) to a sample of positions."""
+    expert-level comparisons (and y) to a sample of positions.
+
+    The oracle evaluates the sampled positions expert by expert, in runs of at
+    most ``max_tokens`` positions on a thread pool (evaluation order only); each
+    run's pairs are compared as they come, so full-size layers are checked in
+    bounded memory."""
     shape = layer.shape
     T = x.shape[0]
+    H = shape.hidden
     assert g["status"] == 0, f"device status {g['status']}"
     if idx is None:
         logits = oracle.router_logits(x, layer.router_w)
@@ -144,82 +159,97 @@ def check_parity(layer: DeviceLayer, x, g, ref=None, idx=None, w=None, tokens=No
     assert np.array_equal(g["dx"], dx), "Q8_0 scales of x differ"
 
     sel = np.arange(T) if tokens is None else np.asarray(tokens)
-    ref = oracle.moe_forward(shape, layer.get_record, x[sel], idx[sel], w[sel], keep_pairs=True)
-    # map oracle pairs of the sampled positions onto GPU pair slots
-    stats = dict(qh_checked=0, qh_unstable=0, qh_flips=0, accd_blocks=0)
-    for (kind, e), pr in ref["pairs"].items():
+    w = np.asarray(w, np.float64)
+    # host copies of the records the sampled positions use, fetched up front
+    for e in np.unique(idx[sel][(idx[sel] >= 0) & (idx[sel] < shape.n_experts)]):
+        layer.get_record("routed", int(e))
+    for s in range(shape.n_shared):
+        layer.get_record("shared", s)
+
+    lock = threading.Lock()
+    stats = dict(qh_checked=0, qh_unstable=0, qh_flips=0, accd_blocks=0, pairs=0)
+    y_delta = np.zeros((sel.size, H))   # linear effect of the GPU's admissible qh steps
+    bound = np.zeros((sel.size, H))     # elementwise bound on |y_gpu - y_oracle|
+    gsz = shape.group_size
+
+    def on_entry(kind, e, pr):
         inter = shape.inter if kind == "routed" else shape.shared_inter
-        for n, tl in enumerate(pr["tokens"]):
-            t = int(sel[tl])
-            if kind == "routed":
-                p = int(g["slot"][t, pr["js"][n]])
-            else:
-                p = int(tabs["offsets"][tabs["uniq"].size + e] + t)
-            if "acc_gu" in g:
-                assert np.array_equal(g["acc_gu"][p, 0, :inter], pr["acc_g"][n]), "gate block dots differ"
-                assert np.array_equal(g["acc_gu"][p, 1, :inter], pr["acc_u"][n]), "up block dots differ"
-            qh_g = g["qh"][p, :inter].astype(np.int64)
-            qh_r = pr["qh"][n].astype(np.int64)
-            st = pr["qh_stable"][n]
-            assert np.array_equal(qh_g[st], qh_r[st]), "requantised h differs where unique"
-            assert np.abs(qh_g - qh_r).max(initial=0) <= 1
+        tl = pr["tokens"]                      # indices into sel
+        ts = sel[tl]
+        if kind == "routed":
+            ps = g["slot"][ts, pr["js"]].astype(np.int64)
+            wt = w[ts, pr["js"]]
+        else:
+            ps = int(tabs["offsets"][tabs["uniq"].size + e]) + ts
+            wt = np.ones(ts.size)
+        if "acc_gu" in g:
+            assert np.array_equal(g["acc_gu"][ps, 0, :inter], pr["acc_g"]), "gate block dots differ"
+            assert np.array_equal(g["acc_gu"][ps, 1, :inter], pr["acc_u"]), "up block dots differ"
+        qh_g = g["qh"][ps, :inter].astype(np.int64)
+        qh_r = pr["qh"].astype(np.int64)
+        st = pr["qh_stable"]
+        assert np.array_equal(qh_g[st], qh_r[st]), "requantised h differs where unique"
+        assert np.abs(qh_g - qh_r).max(initial=0) <= 1
+        # block scale: amax/127 of h, within the h error bound of the oracle
+        nb = inter // 32
+        dh = pr["dh"].astype(np.float64)                                          # [n, nb]
+        ddh = 4.0 * pr["h_err"].reshape(-1, nb, 32).max(axis=2) / 127.0 + np.abs(dh) * 2.0 ** -21
+        assert np.all(np.abs(g["dh"][ps, :nb].astype(np.float64) - dh) <= ddh), "dh outside its bound"
+        blk_ok = (qh_g == qh_r).reshape(-1, nb, 32).all(axis=2)                    # [n, nb]
+        if "acc_d" in g:
+            # bit-exact given the same codes: every block whose 32 h codes the
+            # GPU and the oracle agree on (all of them unless a non-unique
+            # code took its other admissible value)
+            ad = g["acc_d"][ps, :, :nb]                                           # [n, H, nb]
+            ok = np.broadcast_to(blk_ok[:, None, :], ad.shape)
+            assert np.array_equal(ad[ok], pr["acc_d"][ok]), "down block dots differ"
+        # Where the GPU took the other admissible code of a non-unique h
+        # value (asserted above: |dq| <= 1 and only there), the oracle's
+        # output for the GPU's codes is the oracle's own plus the linear
+        # effect of those steps on the down product.  The elementwise bound
+        # covers the unadjusted difference: fp32 evaluation plus the effect
+        # of every +-1 step.
+        rec, sc = layer.get_record(kind, e)
+        wd = oracle.unpack_weight_rows(np.asarray(rec).reshape(-1)[2 * inter * shape.row_bytes(H):],
+                                       H, inter, shape.weight_bits).astype(np.float64)
+        sc = np.asarray(sc, np.float64)
+        if gsz:  # the down matrix's scales: [H][inter/g] after gate and up
+            s_blk = np.repeat(sc[2 * inter * H // gsz:].reshape(H, inter // gsz), gsz // 32, axis=1)
+        else:
+            s_blk = np.repeat(sc[2 * inter:2 * inter + H][:, None], nb, axis=1)
+        wd_s = wd * np.repeat(s_blk, 32, axis=1)                                  # dequantised down weights
+        dqs = (qh_g - qh_r).astype(np.float64)                                     # [n, inter]
+        adj = (wd_s @ (dqs * np.repeat(dh, 32, axis=1)).T).T                       # [n, H]
+        flip = (np.abs(wd_s) @ (np.abs(dqs) * np.repeat(dh + ddh, 32, axis=1)).T).T
+        acc_term = np.einsum("hb,nhb,nb->nh", np.abs(s_blk), np.abs(pr["acc_d"]).astype(np.float64), ddh)
+        term = 4.0 * pr["o_err"] + acc_term + flip
+        # combine rounding (fp32, k + n_shared terms) and fp32 gate weights
+        bnd = np.abs(wt)[:, None] * (term + np.abs(pr["o"]) * (2.0 ** -20 + 2e-6))
+        with lock:
+            np.add.at(y_delta, tl, wt[:, None] * adj)
+            np.add.at(bound, tl, bnd)
             stats["qh_checked"] += qh_g.size
             stats["qh_unstable"] += int((~st).sum())
             stats["qh_flips"] += int((qh_g != qh_r).sum())
-            # block scale: amax/127 of h, within the h error bound of the oracle
-            dh_tol = 4.0 * pr["h_err"][n].reshape(-1, 32).max(axis=1) / 127.0 \
-                + np.abs(pr["dh"][n]).astype(np.float64) * 2.0 ** -21
-            assert np.all(np.abs(g["dh"][p, :inter // 32].astype(np.float64) - pr["dh"][n]) <= dh_tol)
-            if "acc_d" in g:
-                # bit-exact given the same codes: every block whose 32 h codes
-                # the GPU and the oracle agree on (all of them unless a
-                # non-unique code took its other admissible value)
-                blk_ok = (qh_g == qh_r).reshape(-1, 32).all(axis=1)
-                ad = g["acc_d"][p, :, :inter // 32]
-                assert np.array_equal(ad[:, blk_ok], pr["acc_d"][n][:, blk_ok]), "down block dots differ"
-                stats["accd_blocks"] += int(blk_ok.sum())
-    # Where the GPU took the other admissible code of a non-unique h value
-    # (asserted above: |dq| <= 1 and only there), the oracle's output for the
-    # GPU's codes is the oracle's own plus the linear effect of those steps
-    # on the down product; the 1e-3 output tolerance applies against that.
-    # The elementwise bound below covers the unadjusted difference: fp32
-    # evaluation plus the effect of every +-1 step.
-    y_adj = ref["y"].copy()
-    bound = np.zeros_like(ref["y"])
-    gsz = shape.group_size
-    for (kind, e), pr in ref["pairs"].items():
-        inter = shape.inter if kind == "routed" else shape.shared_inter
-        rec, sc = layer.get_record(kind, e)
-        wd = oracle.unpack_weight_rows(np.asarray(rec).reshape(-1)[2 * inter * shape.row_bytes(shape.hidden):],
-                                       shape.hidden, inter, shape.weight_bits).astype(np.float64)
-        sc = np.asarray(sc, np.float64)
-        if gsz:  # the down matrix's scales: [H][inter/g] after gate and up
-            s_blk = np.repeat(sc[2 * inter * shape.hidden // gsz:].reshape(shape.hidden, inter // gsz),
-                              gsz // 32, axis=1)
-        else:
-            s_blk = np.repeat(sc[2 * inter:2 * inter + shape.hidden][:, None], inter // 32, axis=1)
-        wd_s = wd * np.repeat(s_blk, 32, axis=1)        # dequantised down weights
-        for n, tl in enumerate(pr["tokens"]):
-            t = int(sel[tl])
-            if kind == "routed":
-                p = int(g["slot"][t, pr["js"][n]])
-                wt = float(w[t, pr["js"][n]])
-            else:
-                p = int(tabs["offsets"][tabs["uniq"].size + e] + t)
-                wt = 1.0
-            dh = pr["dh"][n].astype(np.float64)
-            ddh = 4.0 * pr["h_err"][n].reshape(-1, 32).max(axis=1) / 127.0 + dh * 2.0 ** -21
-            acc = np.abs(pr["acc_d"][n]).astype(np.float64)
-            dqs = (g["qh"][p, :inter].astype(np.int64) - pr["qh"][n]).astype(np.float64)
-            y_adj[tl] += wt * (wd_s @ (dqs * np.repeat(dh, 32)))
-            flip = (np.abs(wd_s) * (np.abs(dqs) * np.repeat(dh + ddh, 32))[None, :]).sum(axis=1)
-            term = 4.0 * pr["o_err"][n] + (np.abs(s_blk) * acc) @ ddh + flip
-            # combine rounding (fp32, k + n_shared terms) and fp32 gate weights
-            bound[tl] += abs(wt) * (term + np.abs(pr["o"][n]) * (2.0 ** -20 + 2e-6))
-    err = normwise_err(g["y"][sel], y_adj)
-    assert err <= Y_TOL, f"layer output error {err:.3e}"
+            stats["accd_blocks"] += int(blk_ok.sum()) * H
+            stats["pairs"] += tl.size
+
+    n_thr = threads or (_pool_size() if sel.size * shape.hidden > 65536 else 1)
+    with cf.ThreadPoolExecutor(n_thr) as ex:
+        ref = oracle.moe_forward(shape, layer.get_record, x[sel], idx[sel], w[sel], on_entry=on_entry,
+                                 map_fn=ex.map, max_tokens=max_tokens)
+    y_g = g["y"][sel]
+    err = normwise_err(y_g, ref["y"] + y_delta)
+    assert err <= Y_TOL, f"layer output error {err:.3e} (against the oracle for the GPU's h codes)"
     stats["y_err"] = err
-    stats["y_err_unadjusted"] = normwise_err(g["y"][sel], ref["y"])
-    dy = np.abs(g["y"][sel].astype(np.float64) - ref["y"])
+    # against the oracle's own output: the 1e-3 bound holds for int4 and int8
+    # weights; with packed int2 one admissible h step can move y by more
+    # than that, so there only the adjusted comparison above is asserted
+    stats["y_err_unadjusted"] = normwise_err(y_g, ref["y"])
+    if shape.weight_bits != 2:
+        assert stats["y_err_unadjusted"] <= Y_TOL, \
+            f"layer output error {stats['y_err_unadjusted']:.3e} against the oracle's own output"
+    stats["y_err_elementwise_rms_floor"] = elementwise_err(y_g, ref["y"])
+    dy = np.abs(y_g.astype(np.float64) - ref["y"])
     assert np.all(dy <= bound + 1e-30), f"elementwise output bound exceeded by {(dy - bound).max():.3e}"
     return stats

@@ -167,7 +167,7 @@ def test_glm_mtp_verify_t4():
     shape = synth.GLM
     seed = synth.WORKLOADS["glm_mtp_verify_t4"][1]
     L = DeviceLayer(shape, seed, device_weights=True)
-    for call in range(2):
+    for call in range(8):
         att = [0, 0, 0, 0]
         for p in range(4):
             while True:
@@ -184,23 +184,39 @@ def test_glm_mtp_verify_t4():
 
 
 def test_glm_prefill_s2048():
-    """2048 positions: every routing index and table checked, outputs sampled."""
+    """2048 positions: every routing index and table, and every position's
+    output, requantised h codes and scales checked against the oracle."""
     shape = synth.GLM
     seed = synth.WORKLOADS["glm_prefill_s2048"][1]
     L = DeviceLayer(shape, seed, device_weights=True, bias="zero")
     x, _, rej = margin_batch(shape, seed, 0, 2048, L.router_w, L.bias)
     g = L.run(x, dump=False)
-    sample = [0, 1, 777, 1500, 2046, 2047]
-    st = check_parity(L, x, g, tokens=sample)
+    st = check_parity(L, x, g)
     hit = g["n_entries"] - shape.n_shared
     print("prefill unique experts", hit, "rejected", rej, st)
     assert hit == shape.n_experts
+    assert st["pairs"] == 2048 * (shape.top_k + shape.n_shared)
+
+
+def test_glm_shaped_tensor_core_block_dots():
+    """The tensor-core expert path at GLM-5.2 row lengths (hidden 6144,
+    moe_inter 2048) with 16 routed experts and 128 positions, about 64 pairs
+    per expert as in the 2048-position prefill: every int32 gate, up and down
+    block dot product dumped and compared bit for bit."""
+    shape = dataclasses.replace(synth.GLM, n_experts=16, n_groups=4, topk_group=2)
+    seed = synth.WORKLOADS["glm_prefill_s2048"][1]
+    L = DeviceLayer(shape, seed, device_weights=True, bias="zero")
+    x, _, _ = margin_batch(shape, seed, "pf16", 128, L.router_w, L.bias)
+    g = L.run(x, dump=True)
+    st = check_parity(L, x, g)
+    print("glm-shaped tensor-core dump", st)
+    assert st["pairs"] == 128 * (shape.top_k + shape.n_shared)
 
 
 @pytest.mark.parametrize("bits,layer", [(4, 0), (4, 23), (8, 24)])
 def test_glm_stack_layers_b32(bits, layer):
     """Layers of the 24+1 stack at batch 32 with Zipf-skewed correction bias
-    (int8 weights for the multi-token-prediction layer)."""
+    (int8 weights for the multi-token-prediction layer), every position checked."""
     shape = synth.GLM if bits == 4 else synth.GLM_INT8
     seed = synth.WORKLOADS["glm_stack24_mtp1_b32"][1]
     L = DeviceLayer(shape, seed, layer=layer, device_weights=True, bias="zipf")
@@ -209,10 +225,32 @@ def test_glm_stack_layers_b32(bits, layer):
     keep = np.flatnonzero(m >= 1e-4)
     x = np.ascontiguousarray(x[keep])
     g = L.run(x, dump=False)
-    st = check_parity(L, x, g, tokens=[0, len(keep) // 2, len(keep) - 1])
+    st = check_parity(L, x, g)
     counts = g["entry_count"][:-shape.n_shared]
     print("stack layer", layer, "positions", len(keep), "unique", counts.size, "max per expert",
           counts.max(), st)
+
+
+def test_glm_stack_every_layer_step0():
+    """Step 0 of the 24+1-layer stack at batch 32: every layer's routing
+    indices and tables bit-exact for all positions with a routing margin, and
+    one position's output per layer."""
+    seed = synth.WORKLOADS["glm_stack24_mtp1_b32"][1]
+    kept = []
+    for layer in range(25):
+        shape = synth.GLM_INT8 if layer == 24 else synth.GLM
+        L = DeviceLayer(shape, seed, layer=layer, device_weights=True, bias="zipf")
+        x = synth.stack_input(shape, seed, 0, layer)
+        m = oracle.route_margins(oracle.router_logits(x, L.router_w), L.bias, shape)
+        keep = np.flatnonzero(m >= 1e-4)
+        xk = np.ascontiguousarray(x[keep])
+        g = L.run(xk, layer=True)
+        check_parity(L, xk, g, tokens=[layer % len(keep)])
+        kept.append(len(keep))
+        del L, g
+        torch.cuda.empty_cache()
+    print("stack step 0 positions with a margin per layer", kept)
+    assert min(kept) >= 16
 
 
 def test_single_position_edge_cases(tiny):

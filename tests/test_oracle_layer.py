@@ -113,3 +113,30 @@ def test_int2_layer_combine_and_dequantised_path():
         rec, sc = get("shared", 0)
         y[t] += oracle.expert_ffn_dequant_fp64(rec, sc, shape.hidden, shape.shared_inter, 2, x[t:t + 1])[0]
     assert np.allclose(out["y"], y, rtol=1e-9, atol=1e-12 * np.abs(y).max())
+
+
+def test_runs_and_thread_pool_change_nothing(tiny_layer):
+    """Splitting an expert's tokens into runs and evaluating the runs on a
+    thread pool is evaluation order only: outputs, bounds, kept pairs and the
+    per-run callback cover exactly the plain evaluation."""
+    import concurrent.futures as cf
+    L = tiny_layer
+    shape = L["shape"]
+    x = synth.token_batch(shape, 3, "runs", range(13))
+    idx, w = oracle.route(oracle.router_logits(x, L["router_w"]), L["bias"], shape)
+    idx[2, 1] = idx[2, 0]          # a duplicate id: two pairs of one token on one expert
+    plain = oracle.moe_forward(shape, L["get_record"], x, idx, w, keep_pairs=True)
+    seen = []
+    with cf.ThreadPoolExecutor(4) as ex:
+        split = oracle.moe_forward(shape, L["get_record"], x, idx, w, keep_pairs=True, max_tokens=3,
+                                   map_fn=ex.map, on_entry=lambda k, e, o: seen.append((k, e, len(o["tokens"]))))
+    assert np.array_equal(plain["y"], split["y"]) and np.array_equal(plain["y_err"], split["y_err"])
+    assert plain["pairs"].keys() == split["pairs"].keys()
+    for key, pr in plain["pairs"].items():
+        for name in ("tokens", "js", "acc_g", "acc_u", "acc_d", "qh", "dh", "o"):
+            assert np.array_equal(pr[name], split["pairs"][key][name]), (key, name)
+    per_entry = {}
+    for k, e, n in seen:
+        assert n <= 3
+        per_entry[(k, e)] = per_entry.get((k, e), 0) + n
+    assert per_entry == {key: len(pr["tokens"]) for key, pr in plain["pairs"].items()}

@@ -10,6 +10,7 @@ import numpy as np
 import pytest
 
 import oracle
+import synth
 
 GOLD = os.path.join(os.path.dirname(__file__), "golden")
 
@@ -142,3 +143,39 @@ def test_config_validation():
         oracle.route(np.zeros((1, 10)), np.zeros(10, np.float32), cfg(3, 1, 2))
     with pytest.raises(ValueError):
         oracle.route(np.zeros((1, 8)), np.zeros(8, np.float32), cfg(4, 1, 3))
+
+
+def test_designed_exact_ties_select_as_derived_by_hand():
+    """The tie designs used by the GPU tie tests: the oracle's selection on
+    them is the one derived by hand from the lower-id rule (page-4 write-up,
+    'How it works (validated core mechanics)'), and the gate weights are
+    exactly rsf / k (every selected affinity is 1/2)."""
+    from helpers import tie_design
+    for shape in (synth.TINY, synth.GLM):
+        bias, expect = tie_design(shape)
+        logits = np.zeros((3, shape.n_experts))
+        idx, w = oracle.route(logits, bias, shape)
+        assert idx.tolist() == [expect] * 3
+        assert np.all(w == shape.routed_scaling_factor / shape.top_k)
+        # the bias values sit on the 2^-10 grid: 1/2 + b is exact in fp32
+        c32 = np.float32(0.5) + bias
+        assert np.array_equal(c32.astype(np.float64), 0.5 + bias.astype(np.float64))
+
+
+def test_duplicated_group_ties_go_to_the_lower_id():
+    from helpers import duplicate_group, route_margins_except_exact
+    shape = synth.TINY
+    wr, b = duplicate_group(synth.router_weight(shape, 4), synth.router_bias(shape, 4), shape, 0, 1)
+    x = synth.token_batch(shape, 4, "dup", range(40))
+    idx, _ = oracle.route(oracle.router_logits(x, wr), b, shape)
+    both = 0
+    for row in idx:
+        for e in row:
+            if e < 4:      # an expert of group 0 selected ...
+                if e + 4 in row:   # ... with its twin: the lower id comes first
+                    both += 1
+                    assert list(row).index(e) < list(row).index(e + 4)
+            if 4 <= e < 8:         # a group-1 expert only with its group-0 twin before it
+                assert e - 4 in row and list(row).index(e - 4) < list(row).index(e)
+    assert both > 0
+    assert np.all(route_margins_except_exact(oracle.router_logits(x, wr), b, shape) > 0)
