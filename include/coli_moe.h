@@ -87,7 +87,31 @@ typedef struct coli_moe_cfg {
                                        64: one per 64 weights of a row ("gs64",
                                        int4 only: COLI_EUNSUPPORTED with int8
                                        or int2) */
+    int32_t ep_rank;                /* expert-parallel shard of this call   */
+    int32_t ep_size;                /* shards (0 or 1: no sharding)         */
 } coli_moe_cfg;
+
+/* Expert-parallel sharding (colibrì v1.0 README, "Experimental resident CUDA
+ * backend": each expert lives whole on one device; JustVugg/colibri README,
+ * "Local cluster mode": one batch-union request per layer to each worker).
+ * With ep_size = P > 1 a call computes only its shard's part of the layer:
+ *   - routed expert e belongs to shard e mod P.  `weights.experts` and
+ *     `expert_scales` then hold only this shard's experts, in ascending id
+ *     order: expert e (e mod P == ep_rank) is local record e / P;
+ *   - the shared experts belong to shard 0 (the other shards pass no shared
+ *     weights and compute none);
+ *   - the router is not sharded: every shard runs it on the same x and gets
+ *     the same topk_idx / topk_w;
+ *   - routed slots whose expert belongs to another shard are skipped like
+ *     id -1 (no status bit), so the union tables list this shard's experts
+ *     only, and y is the shard's partial output
+ *         y_r[t] = sum_{j: idx[t][j] mod P == r} w_j o_j + [r == 0] sum_s o_s[t];
+ *   - the sum of y_r over the P shards is the layer's output; the caller
+ *     forms it (e.g. one all-reduce of y per layer call).
+ * Requires 0 <= ep_rank < ep_size <= n_experts (COLI_EINVAL otherwise);
+ * ep_size 0 or 1 needs ep_rank 0.  The workspace size depends on the shard
+ * (shard 0 holds the shared experts' pairs), so size it with the shard's own
+ * cfg. */
 
 /* Expert weights.  One expert "record" is its three matrices stored adjacent
  * (colibrì "JustVugg/colibri" README, "Never wait for the disk twice": an
@@ -102,7 +126,8 @@ typedef struct coli_moe_cfg {
  *                  4j .. 4j+3, element 4j+m in bits 2m and 2m+1, each stored
  *                  as code + 2 (codes in [-2, 1]).
  * Records are consecutive: expert e starts at experts + e * record_bytes,
- * record_bytes = (2*Ie*H + H*Ie) * weight_bits / 8.
+ * record_bytes = (2*Ie*H + H*Ie) * weight_bits / 8 (with expert-parallel
+ * sharding, e is the local record index e / ep_size; see below).
  * Scales are fp32 per output row, consecutive per expert:
  *     expert_scales[e * (2*I + H) + {0..I-1: gate, I..2I-1: up, 2I..: down}]
  * and likewise shared_scales with shared_inter.
@@ -203,6 +228,40 @@ int coli_moe_status(void* ws, cudaStream_t stream, uint32_t* status);
 
 /* Static text for a return code. */
 const char* coli_moe_strerror(int code);
+
+/* ---- a stack of layers ---------------------------------------------------
+ * One decode step through a stack of MoE layers with the hidden state kept
+ * on the device between layers (JustVugg/colibri README, "Never wait for the
+ * disk twice": the residual stream stays resident on the GPU across layers,
+ * COLI_CUDA_PIPE=2).  Layer l runs coli_moe_layer on xs[l]; then a small
+ * kernel writes the next layer's input
+ *     xs[l+1] = xs[l] + residual[l]            (add_output == 0)
+ *     xs[l+1] = (xs[l] + y[l]) + residual[l]   (add_output == 1)
+ * in fp32.  Nothing returns to the host between layers; the whole step can
+ * be captured once in a CUDA graph and replayed.
+ *   layers    [n_layers] per-layer config, weights, router weight and bias;
+ *             every layer has the same hidden and top_k (COLI_EINVAL
+ *             otherwise); weight formats and the other shapes may differ
+ *   xs        [n_layers + 1][T][H] fp32: xs[0] is read, xs[1..] written
+ *   residual  [n_layers][T][H] fp32 (NULL: zero)
+ *   topk_idx  [n_layers][T][k] int32 out, topk_w [n_layers][T][k] fp32 out
+ *   y         [n_layers][T][H] fp32 out: each layer's output
+ *   ws        one workspace of at least the largest
+ *             coli_moe_workspace_size(layers[l].cfg, T) (COLI_EWORKSPACE
+ *             otherwise), prepared with coli_moe_workspace_init
+ * Arguments are checked for every layer before anything is enqueued; status
+ * bits of all layers accumulate in the workspace's status word. */
+typedef struct coli_moe_stack_layer {
+    coli_moe_cfg     cfg;
+    coli_moe_weights weights;
+    const float*     router_w;   /* [E][H] */
+    const float*     corr_bias;  /* [E]    */
+} coli_moe_stack_layer;
+
+int coli_moe_stack_forward(const coli_moe_stack_layer* layers, int32_t n_layers, int32_t T,
+                           float* xs, const float* residual, int32_t add_output,
+                           int32_t* topk_idx, float* topk_w, float* y,
+                           void* ws, size_t ws_bytes, cudaStream_t stream);
 
 /* ---- inspection (tests) -------------------------------------------------
  * Byte offsets, inside the workspace of coli_moe_workspace_size(cfg, max_T),

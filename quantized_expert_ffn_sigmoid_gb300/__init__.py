@@ -30,6 +30,7 @@ EXPORTS = (
     "coli_moe_quantize_act", "coli_moe_forward", "coli_moe_dispatch", "coli_moe_experts",
     "coli_moe_status", "coli_moe_strerror", "coli_moe_workspace_layout",
     "coli_moe_forward_dump", "coli_moe_forward_static", "coli_moe_layer",
+    "coli_moe_stack_forward",
 )
 STATIC_WS_BYTES = 24 << 20
 
@@ -40,18 +41,26 @@ class Cfg(ctypes.Structure):
                 ("top_k", ctypes.c_int32), ("inter", ctypes.c_int32),
                 ("n_shared", ctypes.c_int32), ("shared_inter", ctypes.c_int32),
                 ("weight_bits", ctypes.c_int32), ("routed_scaling_factor", ctypes.c_float),
-                ("group_size", ctypes.c_int32)]
+                ("group_size", ctypes.c_int32), ("ep_rank", ctypes.c_int32), ("ep_size", ctypes.c_int32)]
+    _OPTIONAL = ("group_size", "ep_rank", "ep_size")
 
     @classmethod
-    def of(cls, shape) -> "Cfg":
+    def of(cls, shape, ep_rank: int = 0, ep_size: int = 0) -> "Cfg":
         """From any object with the same field names (e.g. synth.LayerShape);
-        a missing group_size means per-row scales."""
-        return cls(*(getattr(shape, f, 0) if f == "group_size" else getattr(shape, f) for f, _ in cls._fields_))
+        a missing group_size means per-row scales.  ``ep_rank`` / ``ep_size``
+        select one shard of an expert-parallel layer (0 / 0: the whole layer)."""
+        vals = {"ep_rank": ep_rank, "ep_size": ep_size}
+        return cls(*(vals[f] if f in vals else getattr(shape, f, 0) if f in cls._OPTIONAL else getattr(shape, f)
+                     for f, _ in cls._fields_))
 
 
 class Weights(ctypes.Structure):
     _fields_ = [("experts", ctypes.c_void_p), ("expert_scales", ctypes.c_void_p),
                 ("shared", ctypes.c_void_p), ("shared_scales", ctypes.c_void_p)]
+
+
+class StackLayer(ctypes.Structure):
+    _fields_ = [("cfg", Cfg), ("weights", Weights), ("router_w", ctypes.c_void_p), ("corr_bias", ctypes.c_void_p)]
 
 
 class WsLayout(ctypes.Structure):
@@ -81,6 +90,8 @@ def _load():
         "coli_moe_forward_dump": ([CP, WP, P, I32, P, P, P, P, S, P, P, P], ctypes.c_int),
         "coli_moe_forward_static": ([CP, WP, P, I32, P, P, P, P], ctypes.c_int),
         "coli_moe_layer": ([CP, WP, P, I32, P, P, P, P, P, P, S, P], ctypes.c_int),
+        "coli_moe_stack_forward": ([ctypes.POINTER(StackLayer), I32, I32, P, P, I32, P, P, P, P, S, P],
+                                   ctypes.c_int),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -213,3 +224,35 @@ def coli_moe_forward_static(cfg, weights: Weights, x, topk_idx, topk_w, y, strea
     _check(lib.coli_moe_forward_static(ctypes.byref(_cfg(cfg)), ctypes.byref(weights), _ptr(x), x.shape[0],
                                        _ptr(topk_idx), _ptr(topk_w), _ptr(y), _stream(stream)),
            "coli_moe_forward_static")
+
+
+def stack_layers(layers):
+    """A ctypes array of StackLayer from (cfg, weights, router_w, corr_bias)
+    tuples (keep the tensors alive)."""
+    arr = (StackLayer * len(layers))()
+    for i, (cfg, w, wr, b) in enumerate(layers):
+        arr[i] = StackLayer(_cfg(cfg), w, wr.data_ptr(), b.data_ptr())
+    return arr
+
+
+def coli_moe_stack_forward(layers, xs, residual, topk_idx, topk_w, y, ws, add_output=False, stream=None):
+    """One step through a stack of layers (``layers`` from stack_layers):
+    xs [L+1, T, H] (xs[0] read, the rest written), residual [L, T, H] or
+    None, topk_idx / topk_w [L, T, k] and y [L, T, H] written."""
+    n, T = len(layers), xs.shape[1]
+    _check(lib.coli_moe_stack_forward(layers, n, T, _ptr(xs), _ptr(residual), int(bool(add_output)),
+                                      _ptr(topk_idx), _ptr(topk_w), _ptr(y), _ptr(ws), ws.numel(),
+                                      _stream(stream)), "coli_moe_stack_forward")
+
+
+def capture_stack_step(layers, xs, residual, topk_idx, topk_w, y, ws, add_output=False):
+    """The stack step captured once as a CUDA graph (torch.cuda.CUDAGraph);
+    ``graph.replay()`` runs it again on the same buffers.  Runs the step once
+    first, outside capture (the first call of some kernels sets attributes)."""
+    import torch
+    coli_moe_stack_forward(layers, xs, residual, topk_idx, topk_w, y, ws, add_output)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, capture_error_mode="thread_local"):
+        coli_moe_stack_forward(layers, xs, residual, topk_idx, topk_w, y, ws, add_output)
+    return g

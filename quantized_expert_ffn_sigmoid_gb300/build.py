@@ -9,7 +9,7 @@ import subprocess
 HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 LIB = os.path.join(HERE, "libcolimoe.so")
-SOURCES = ["api.cu", "route.cu", "dispatch.cu", "experts.cu", "gemv.cu", "decode.cu", "prefill.cu", "smallbatch.cu", "static_ws.cu"]
+SOURCES = ["api.cu", "route.cu", "dispatch.cu", "experts.cu", "gemv.cu", "decode.cu", "prefill.cu", "smallbatch.cu", "static_ws.cu", "stack.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xptxas", "-v"]
 

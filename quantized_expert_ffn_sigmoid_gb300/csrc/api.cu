@@ -54,6 +54,9 @@ int check_cfg(const coli_moe_cfg* c) {
   const int imax = c->inter > c->shared_inter ? c->inter : c->shared_inter;
   if (4 * row_bytes(imax, c->weight_bits) > SB) return COLI_EUNSUPPORTED;
   if (c->hidden % RB) return COLI_EUNSUPPORTED;
+  // expert-parallel shard: 0 <= ep_rank < ep_size <= E, or no sharding
+  if (c->ep_size < 0 || c->ep_size > c->n_experts || c->ep_rank < 0) return COLI_EINVAL;
+  if (c->ep_rank >= (c->ep_size > 1 ? c->ep_size : 1)) return COLI_EINVAL;
   return COLI_OK;
 }
 
@@ -67,6 +70,8 @@ bool fast_paths(const coli_moe_cfg& c) { return per_row(c) && c.weight_bits != 2
 
 coli_moe_cfg normalized(const coli_moe_cfg* c) {
   coli_moe_cfg n = *c;
+  if (n.ep_size <= 1) n.ep_size = 1;
+  if (n.ep_rank != 0) n.n_shared = 0;   // the shared experts belong to shard 0
   if (n.n_shared == 0) n.shared_inter = n.inter;
   return n;
 }
@@ -286,7 +291,9 @@ int coli_moe_layer(const coli_moe_cfg* cfg, const coli_moe_weights* weights, con
   Layout L;
   if ((rc = check_ws(c, T, ws, ws_bytes, &L))) return rc;
   uint8_t* w8 = static_cast<uint8_t*>(ws);
-  if (T == 1 && decode_route_fits(c)) {
+  if (T == 1 && c.ep_size == 1 && decode_route_fits(c)) {
+    // (a shard of an expert-parallel layer routes first: its experts are a
+    // subset of the selection, which the fused kernel's schedule assumes whole)
     const int n_sm = sm_count();
     if (n_sm <= 0) return COLI_ECUDA;
     const ExpertParams P = expert_params(c, weights, topk_w, y, w8, L, nullptr, nullptr);

@@ -36,6 +36,17 @@ constexpr uint32_t SPIN_LIMIT = 1u << 22;  // bounded waits (about a second or m
 
 __host__ __device__ inline int row_bytes(int k, int bits) { return bits == 4 ? k / 2 : bits == 2 ? k / 4 : k; }
 
+// Expert-parallel sharding: with ep_size > 1 a call computes the routed
+// experts e with e mod ep_size == ep_rank, stored as local record e / ep_size.
+__host__ __device__ inline bool ep_owned(const coli_moe_cfg& c, int e) {
+  return c.ep_size <= 1 || e % c.ep_size == c.ep_rank;
+}
+__host__ __device__ inline int ep_local(const coli_moe_cfg& c, int e) { return c.ep_size <= 1 ? e : e / c.ep_size; }
+// routed records held by this shard
+__host__ __device__ inline int ep_records(const coli_moe_cfg& c) {
+  return c.ep_size <= 1 ? c.n_experts : (c.n_experts - c.ep_rank + c.ep_size - 1) / c.ep_size;
+}
+
 // K ranges of the tiled router GEMM (calls of more than ROUTE_GEMV_MAX_T
 // positions): about 1024 CTAs of 64 x 64 logits, at least 192 K elements
 // each; the partial logits of every range are summed in range order.

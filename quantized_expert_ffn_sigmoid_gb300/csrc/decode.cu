@@ -114,7 +114,7 @@ __device__ __forceinline__ const uint8_t* dec_record(const ExpertParams& P, int 
   const int H = c.hidden, bits = c.weight_bits;
   const bool routed = expert < c.n_experts;
   const int I = routed ? c.inter : c.shared_inter;
-  const int e = routed ? expert : expert - c.n_experts;
+  const int e = routed ? ep_local(c, expert) : expert - c.n_experts;
   const size_t rec = (size_t)2 * I * row_bytes(H, bits) + (size_t)H * row_bytes(I, bits);
   const size_t nsc = GS ? (size_t)3 * I * (H / 64) : (size_t)2 * I + H;
   *inter = I;
@@ -528,8 +528,9 @@ decode_layer_kernel(ExpertParams P, const float* __restrict__ x, const int32_t* 
     // distinct valid ids ascending, pairs by (id, slot), then shared
     if (warp == DK_NW - 1) {
       const int e = lane < k ? topk_idx[lane] : -1;
-      const bool valid = lane < k && e >= 0 && e < E;
-      if (blockIdx.x == 0 && __any_sync(0xffffffffu, lane < k && !valid && e != -1) && lane == 0)
+      const bool inrange = lane < k && e >= 0 && e < E;
+      const bool valid = inrange && ep_owned(c, e);   // another shard's expert: skipped
+      if (blockIdx.x == 0 && __any_sync(0xffffffffu, lane < k && !inrange && e != -1) && lane == 0)
         atomicOr(status, COLI_STATUS_BADIDX);
       const int key = valid ? (e << 8) | lane : 0x7fffffff;
       int rank = 0, before = 0, cnt = 0;
@@ -677,7 +678,7 @@ decode_layer_kernel(ExpertParams P, const float* __restrict__ x, const int32_t* 
   };
   float gsc[2][4], gsn[2][4];
   if constexpr (GS) {
-    if (ngr > 0) load_gs(0, gsn);
+    if (ngr > 0 && n_ent > 0) load_gs(0, gsn);
   }
   if (ngr > 0) {
     if (lane == 0)

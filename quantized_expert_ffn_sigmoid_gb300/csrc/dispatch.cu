@@ -123,8 +123,11 @@ __global__ void __launch_bounds__(PREP_THREADS) prep_kernel(PrepParams P) {
   bool badidx = false;
   for (int p = tid; p < npair; p += PREP_THREADS) {
     int e = P.idx[p];
-    if (e >= 0 && e < E) atomicAdd(&cnt[e], 1);
-    else if (e != -1) badidx = true;
+    if (e >= 0 && e < E) {
+      if (ep_owned(c, e)) atomicAdd(&cnt[e], 1);   // another shard's expert: skipped
+    } else if (e != -1) {
+      badidx = true;
+    }
   }
   if (__any_sync(0xffffffffu, badidx) && lane == 0) atomicOr(status, COLI_STATUS_BADIDX);
   __syncthreads();
@@ -163,7 +166,7 @@ __global__ void __launch_bounds__(PREP_THREADS) prep_kernel(PrepParams P) {
     __syncwarp();
     const int p = base + tid;
     const int e = p < npair ? P.idx[p] : -1;
-    const bool valid = e >= 0 && e < E;
+    const bool valid = e >= 0 && e < E && ep_owned(c, e);
     const unsigned same = __match_any_sync(0xffffffffu, valid ? e : -1);
     const int lrank = __popc(same & ((1u << lane) - 1u));
     if (valid && lrank == 0) wcnt[warp * E + e] = (uint16_t)__popc(same);
@@ -287,8 +290,9 @@ __global__ void __launch_bounds__(256) prep_small_kernel(PrepParams P) {
   bool badidx = false;
   for (int p = lane; p < npair; p += 32) {
     const int e = P.idx[p];
-    const bool valid = e >= 0 && e < E;
-    if (!valid && e != -1) badidx = true;
+    const bool inrange = e >= 0 && e < E;
+    if (!inrange && e != -1) badidx = true;
+    const bool valid = inrange && ep_owned(c, e);   // another shard's expert: skipped
     key[p] = valid ? (e << 8) | p : 0x7fffffff;
   }
   if (__any_sync(0xffffffffu, badidx) && lane == 0) atomicOr(status, COLI_STATUS_BADIDX);

@@ -143,8 +143,9 @@ __device__ __forceinline__ const uint8_t* entry_record(const ExpertParams& P, in
   if (expert < c.n_experts) {
     const size_t rec = (size_t)2 * c.inter * row_bytes(H, bits) + (size_t)H * row_bytes(c.inter, bits);
     *inter_out = c.inter;
-    *scales_out = P.expert_scales + (size_t)expert * scale_count(c, c.inter);
-    return P.experts + (size_t)expert * rec;
+    const int e = ep_local(c, expert);
+    *scales_out = P.expert_scales + (size_t)e * scale_count(c, c.inter);
+    return P.experts + (size_t)e * rec;
   }
   const int s = expert - c.n_experts;
   const size_t rec = (size_t)2 * c.shared_inter * row_bytes(H, bits) + (size_t)H * row_bytes(c.shared_inter, bits);
@@ -578,6 +579,15 @@ __global__ void __launch_bounds__(EXPERT_THREADS, 1) experts_kernel(ExpertParams
       S.t_offset[i] = eo[i];
       if (i < n_ent) { S.t_count[i] = ec[i]; S.t_expert[i] = ee[i]; }
     }
+  }
+  if (nB == 0) {
+    // no entry at all (every slot skipped and no shared expert, e.g. a shard
+    // of an expert-parallel layer that owns none of the call's experts): the
+    // combine below never runs, so y = 0 is written here
+    const size_t n = (size_t)P.L.T * P.cfg.hidden;
+    for (size_t i = (size_t)blockIdx.x * EXPERT_THREADS + tid; i < n; i += (size_t)gridDim.x * EXPERT_THREADS)
+      P.y[i] = 0.f;
+    return;
   }
   if (tid == 0) {
     for (int i = 0; i < NS; ++i) { mbar_init(&S.full[i], 1); mbar_init(&S.empty[i], NCW); }

@@ -311,7 +311,7 @@ __global__ void __launch_bounds__(PF_THREADS2, 1) pf_gemm(const __grid_constant_
     it.nt = local % ntn;
     it.ntok = min(PF_N, cnt - it.nt * PF_N);
     it.pair0 = e_off[lo] + it.nt * PF_N;
-    it.rec = it.routed ? e_exp[lo] : e_exp[lo] - E;
+    it.rec = it.routed ? ep_local(P.cfg, e_exp[lo]) : e_exp[lo] - E;
     it.nch = (GU ? H : it.inter) / PF_CK;
     return it;
   };
@@ -634,10 +634,10 @@ cudaError_t run_prefill(const ExpertParams& P, int T, int n_sm, cudaStream_t st,
   const int H = c.hidden, E = c.n_experts, I = c.inter, Is = c.shared_inter, ns = c.n_shared;
   const uint32_t kcb = PF_CK * BITS / 8;
   PfMaps gu{}, dn{};
-  bool ok = encode_rows(&gu.w, P.experts, (size_t)H * BITS / 8, (size_t)E * 3 * I, kcb, PF_M) &&
+  bool ok = encode_rows(&gu.w, P.experts, (size_t)H * BITS / 8, (size_t)ep_records(c) * 3 * I, kcb, PF_M) &&
             encode_rows(&gu.act, P.ws + L.o, H, (size_t)T * c.top_k, PF_CK, PF_N) &&
             encode_rows(&gu.act_sh, P.ws + L.qx, H, T, PF_CK, PF_N) &&
-            encode_rows(&dn.w, P.experts, (size_t)I * BITS / 8, (size_t)E * 3 * H, kcb, PF_M) &&
+            encode_rows(&dn.w, P.experts, (size_t)I * BITS / 8, (size_t)ep_records(c) * 3 * H, kcb, PF_M) &&
             encode_rows(&dn.act, P.ws + L.qh, L.imax, L.P, PF_CK, PF_N);
   if (ok && ns > 0) {
     ok = encode_rows(&gu.w_sh, P.shared, (size_t)H * BITS / 8, (size_t)ns * 3 * Is, kcb, PF_M) &&

@@ -280,7 +280,7 @@ __global__ void __launch_bounds__(SB_THREADS, 1) sb_gemm(const __grid_constant__
     d.pair0 = t_off[lo] + tg * cap;
     const int e = t_exp[lo];
     d.shared = e >= E;
-    d.ex = d.shared ? e - E : e;
+    d.ex = d.shared ? e - E : ep_local(P.cfg, e);
     d.inter = d.shared ? c.shared_inter : c.inter;
     d.chunks = (GU ? H : d.inter) / ck;
     return d;
@@ -555,8 +555,8 @@ cudaError_t run_sb(const ExpertParams& P, int n_sm, cudaStream_t st, bool dump) 
   if (!sb_plan(c, P.L, true, &pg) || !sb_plan(c, P.L, false, &pd)) return cudaErrorInvalidValue;
   const size_t rb_h = (size_t)H * BITS / 8;
   SbMaps gu{}, dn{};
-  bool ok = encode_rows(&gu.w, P.experts, rb_h, (size_t)E * 3 * I, pg.swb, 32, pg.swb == 128) &&
-            encode_rows(&dn.w, P.experts, (size_t)I * BITS / 8, (size_t)E * 3 * H, pd.swb, 32, pd.swb == 128);
+  bool ok = encode_rows(&gu.w, P.experts, rb_h, (size_t)ep_records(c) * 3 * I, pg.swb, 32, pg.swb == 128) &&
+            encode_rows(&dn.w, P.experts, (size_t)I * BITS / 8, (size_t)ep_records(c) * 3 * H, pd.swb, 32, pd.swb == 128);
   if (ok && ns > 0) {
     ok = encode_rows(&gu.w_sh, P.shared, rb_h, (size_t)ns * 3 * Is, pg.swb, 32, pg.swb == 128) &&
          encode_rows(&dn.w_sh, P.shared, (size_t)Is * BITS / 8, (size_t)ns * 3 * H, pd.swb, 32, pd.swb == 128);

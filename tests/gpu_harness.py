@@ -62,14 +62,19 @@ class DeviceLayer:
         return self._host[key]
 
     # ------------------------------------------------------------------ runs
-    def run(self, x: np.ndarray, dump=True, ws=None, route=True, idx=None, w=None, layer=False):
+    def run(self, x: np.ndarray, dump=True, ws=None, route=True, idx=None, w=None, layer=False, cfg=None,
+            W=None, shape=None):
         """Route (unless idx/w given) and forward; returns the GPU observables.
-        ``layer``: one coli_moe_layer call (router and experts together)."""
-        shape, dev = self.shape, self.dev
+        ``layer``: one coli_moe_layer call (router and experts together).
+        ``cfg`` / ``W`` / ``shape``: another config and weights of this
+        layer (e.g. one shard of an expert-parallel layer)."""
+        shape, dev = shape or self.shape, self.dev
+        cfg_ = self.cfg if cfg is None else cfg
+        W_ = self.W if W is None else W
         T, k = x.shape[0], shape.top_k
         xd = torch.from_numpy(np.ascontiguousarray(x, np.float32)).to(dev)
         if ws is None:
-            ws = cm.new_workspace(self.cfg, T)
+            ws = cm.new_workspace(cfg_, T)
         if layer:
             idx_d = torch.full((T, k), -7, dtype=torch.int32, device=dev)
             w_d = torch.full((T, k), -7.0, dtype=torch.float32, device=dev)
@@ -77,23 +82,23 @@ class DeviceLayer:
         elif route:
             idx_d = torch.full((T, k), -7, dtype=torch.int32, device=dev)
             w_d = torch.full((T, k), -7.0, dtype=torch.float32, device=dev)
-            cm.coli_moe_route(self.cfg, xd, self.wr_d, self.bias_d, idx_d, w_d, ws)
+            cm.coli_moe_route(cfg_, xd, self.wr_d, self.bias_d, idx_d, w_d, ws)
         else:
             idx_d = torch.from_numpy(np.ascontiguousarray(idx, np.int32)).to(dev)
             w_d = torch.from_numpy(np.ascontiguousarray(w, np.float32)).to(dev)
         y = torch.full((T, shape.hidden), float("nan"), dtype=torch.float32, device=dev)
-        L = cm.coli_moe_workspace_layout(self.cfg, T)
+        L = cm.coli_moe_workspace_layout(cfg_, T)
         P = T * k + shape.n_shared * T
         imax = max(shape.inter, shape.shared_inter if shape.n_shared else 0)
         acc_gu = acc_d = None
         if layer:
-            cm.coli_moe_layer(self.cfg, self.W, xd, self.wr_d, self.bias_d, idx_d, w_d, y, ws)
+            cm.coli_moe_layer(cfg_, W_, xd, self.wr_d, self.bias_d, idx_d, w_d, y, ws)
         elif dump:
             acc_gu = torch.zeros((P, 2, imax, shape.hidden // 32), dtype=torch.int32, device=dev)
             acc_d = torch.zeros((P, shape.hidden, imax // 32), dtype=torch.int32, device=dev)
-            cm.coli_moe_forward_dump(self.cfg, self.W, xd, idx_d, w_d, y, ws, acc_gu, acc_d)
+            cm.coli_moe_forward_dump(cfg_, W_, xd, idx_d, w_d, y, ws, acc_gu, acc_d)
         else:
-            cm.coli_moe_forward(self.cfg, self.W, xd, idx_d, w_d, y, ws)
+            cm.coli_moe_forward(cfg_, W_, xd, idx_d, w_d, y, ws)
         status = cm.coli_moe_status(ws)
         wsh = ws.cpu().numpy()
 

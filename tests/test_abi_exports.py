@@ -94,3 +94,16 @@ def test_weight_bits_host_checks(lib):
                 dataclasses.replace(synth.GLM, weight_bits=3),
                 dataclasses.replace(synth.GLM, weight_bits=1)):
         assert cm.coli_moe_workspace_size(cm.Cfg.of(bad), 4) == 0
+
+
+def test_expert_parallel_host_checks(lib):
+    # shard 0 holds the shared experts' pairs, the other shards do not; the
+    # shard index must lie in [0, ep_size), ep_size in [0, n_experts]
+    import synth
+    import quantized_expert_ffn_sigmoid_gb300 as cm
+    whole = cm.coli_moe_workspace_size(cm.Cfg.of(synth.GLM), 32)
+    assert cm.coli_moe_workspace_size(cm.Cfg.of(synth.GLM, 0, 1), 32) == whole
+    assert cm.coli_moe_workspace_size(cm.Cfg.of(synth.GLM, 0, 4), 32) == whole
+    assert 0 < cm.coli_moe_workspace_size(cm.Cfg.of(synth.GLM, 3, 4), 32) < whole
+    for rank, size in ((4, 4), (-1, 2), (1, 1), (1, 0), (0, 257), (0, -2)):
+        assert cm.coli_moe_workspace_size(cm.Cfg.of(synth.GLM, rank, size), 32) == 0, (rank, size)
