@@ -81,7 +81,8 @@ __host__ __device__ inline size_t align_up(size_t v, size_t a) { return (v + a -
 struct Layout {
   int T, P, n_ent_max, n_tiles, imax;
   size_t status, route_words, counters, hdr, ent_expert, ent_count, ent_offset, ent_item_a,
-         ent_item_b, pair_token, pair_j, slot, route_part, qx, dx, xs, qh, dh, hs, o, total;
+         ent_item_b, pair_token, pair_j, slot, route_part, qx, dx, xs, qh, dh, hs, o,
+         pf_xs, pf_hb, pf_hs, total;
 };
 // Table header (ints at Layout::hdr)
 enum HdrField { H_NENT = 0, H_NUNIQ, H_NA, H_NB, H_BTARGET, H_NPAIRS, H_FIELDS = 8 };
@@ -121,6 +122,13 @@ __host__ __device__ inline Layout make_layout(const coli_moe_cfg& c, int T) {
   L.dh = take(4 * (size_t)L.P * (L.imax / QB));
   L.hs = take(4 * (size_t)L.P * (L.imax / QB));
   L.o = take(4 * (size_t)L.P * H);
+  // tensor-core path only (calls of PF_MIN_T or more positions): activation
+  // scales per pair, transposed [H/32][P]; h codes widened to fp16 [P][imax];
+  // h scales transposed [imax/32][P]
+  const bool pf = T >= PF_MIN_T;
+  L.pf_xs = take(pf ? 4 * (size_t)(H / QB) * L.P : 0);
+  L.pf_hb = take(pf ? 2 * (size_t)L.P * L.imax : 0);
+  L.pf_hs = take(pf ? 4 * (size_t)(L.imax / QB) * L.P : 0);
   L.total = off;
   return L;
 }

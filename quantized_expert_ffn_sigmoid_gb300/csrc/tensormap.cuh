@@ -41,4 +41,21 @@ inline bool encode_rows(CUtensorMap* m, const void* base, size_t row_bytes, size
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// The same with an explicit swizzle mode: with 64-byte rows and
+// CU_TENSOR_MAP_SWIZZLE_64B, the 16-byte chunk c of row r lands at chunk
+// c ^ ((r >> 1) & 3) (the destination must be 512-byte aligned); with 128-byte
+// rows and CU_TENSOR_MAP_SWIZZLE_128B at c ^ (r & 7) (1024-byte aligned).
+inline bool encode_rows_sw(CUtensorMap* m, const void* base, size_t row_bytes, size_t rows, uint32_t box_bytes,
+                           uint32_t box_rows, CUtensorMapSwizzle sw) {
+  auto fn = encode_fn();
+  if (!fn || rows == 0) return false;
+  const cuuint64_t dims[2] = {(cuuint64_t)row_bytes, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)row_bytes};
+  const cuuint32_t box[2] = {box_bytes, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace colimoe
