@@ -82,13 +82,15 @@ struct PfParams {
 };
 
 // Shared memory of pf_gemm: the stage ring (per stage: two raw weight tiles
-// of 128 rows x PF_SBK blocks, swizzled; the B tile as PF_KS / 8 groups of
-// [PF_NMAX pairs][8 fp16]), then the column-scale ring and the barriers.
+// of 128 rows x PF_SBK blocks, swizzled; the B tile as PF_KS / 64 chunks of
+// [PF_NMAX pairs][64 fp16] in the 128-byte-swizzled K-major layout: 128-byte
+// rows, the 16-byte unit c of row r at unit c ^ (r % 8), 8-row atoms of
+// 1024 bytes), then the column-scale ring and the barriers.
 __host__ __device__ constexpr int pf_nst(int bits) { return bits == 4 ? 4 : 3; }
 __host__ __device__ constexpr uint32_t pf_raw_row(int bits) { return (uint32_t)PF_KS * bits / 8; }  // 64 / 128 B
 __host__ __device__ constexpr uint32_t pf_raw_tile(int bits) { return PF_M * pf_raw_row(bits); }
-constexpr uint32_t PF_BGRP = (uint32_t)PF_NMAX * 16;  // one 8-element K group of B (LBO)
-constexpr uint32_t PF_BTILE = (PF_KS / 8) * PF_BGRP;  // 16 KB
+constexpr uint32_t PF_BCHUNK = (uint32_t)PF_NMAX * 128;  // one 64-element K chunk of B (8 KB)
+constexpr uint32_t PF_BTILE = (PF_KS / 64) * PF_BCHUNK;  // 16 KB
 __host__ __device__ constexpr uint32_t pf_stage(int bits) { return 2 * pf_raw_tile(bits) + PF_BTILE; }
 __host__ __device__ constexpr size_t pf_off_sc(int bits) { return (size_t)pf_nst(bits) * pf_stage(bits); }
 __host__ __device__ constexpr size_t pf_off_bar(int bits) {
@@ -96,11 +98,18 @@ __host__ __device__ constexpr size_t pf_off_bar(int bits) {
 }
 __host__ __device__ constexpr size_t pf_smem(int bits) { return pf_off_bar(bits) + 512; }
 
-__device__ __forceinline__ uint64_t umma_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+// Shared-memory matrix descriptor of a K-major operand in the 128-byte
+// swizzled layout: 8-row atoms 1024 bytes apart (stride byte offset), the
+// leading byte offset unused (1), descriptor version 1, layout type 2 (128-byte
+// swizzle).  A K16 slice at byte offset 32 k inside the 128-byte span is
+// addressed by adding that offset to the start address (the swizzle is applied
+// to the address bits, so the atom must be 1024-byte aligned).
+__device__ __forceinline__ uint64_t umma_desc_sw128(uint32_t saddr) {
   uint64_t d = (uint64_t)((saddr >> 4) & 0x3FFF);
-  d |= (uint64_t)((lbo >> 4) & 0x3FFF) << 16;
-  d |= (uint64_t)((sbo >> 4) & 0x3FFF) << 32;
-  d |= (uint64_t)1 << 46;  // descriptor version of this architecture; no swizzle
+  d |= (uint64_t)1 << 16;
+  d |= (uint64_t)(1024 >> 4) << 32;
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)2 << 61;
   return d;
 }
 
@@ -161,16 +170,6 @@ __device__ __forceinline__ void setmaxnreg_inc() { asm volatile("setmaxnreg.inc.
 template <uint32_t N>
 __device__ __forceinline__ void setmaxnreg_dec() { asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N)); }
 
-// (a0, a1) = (d0 * v0 + a0, d1 * v1 + a1), each rounded once: one paired fp32 FMA
-__device__ __forceinline__ void ffma2(float& a0, float& a1, float d0, float d1, float v0, float v1) {
-  asm("{\n\t.reg .b64 ra, rb, rc;\n\t"
-      "mov.b64 ra, {%2, %3};\n\t"
-      "mov.b64 rb, {%4, %5};\n\t"
-      "mov.b64 rc, {%0, %1};\n\t"
-      "fma.rn.f32x2 rc, ra, rb, rc;\n\t"
-      "mov.b64 {%0, %1}, rc;\n\t}"
-      : "+f"(a0), "+f"(a1) : "f"(d0), "f"(d1), "f"(v0), "f"(v1));
-}
 
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
   uint32_t d;
@@ -381,9 +380,9 @@ __global__ void __launch_bounds__(PF_THREADS, 1) pf_gemm(const __grid_constant__
           tma_load_2d(dst, wmap, st * (int)RAW_ROW, row0, &full[s]);
           tma_load_2d(dst + RAW_TILE, wmap, st * (int)RAW_ROW, row1, &full[s]);
           uint8_t* bdst = dst + 2 * RAW_TILE;
-#pragma unroll 1
-          for (int g = 0; g < PF_KS / 8; ++g)
-            tma_load_2d(bdst + (size_t)g * PF_BGRP, &maps.b, st * PF_KS + g * 8, it.pair0, &full[s]);  // x in fp16 elements
+#pragma unroll
+          for (int c2 = 0; c2 < PF_KS / 64; ++c2)  // x in fp16 elements
+            tma_load_2d(bdst + (size_t)c2 * PF_BCHUNK, &maps.b, st * PF_KS + c2 * 64, it.pair0, &full[s]);
         }
       }
       // every copy issued has landed before the CTA can exit (the last phase
@@ -402,7 +401,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1) pf_gemm(const __grid_constant__
         for (int st = 0; st < it.nst; ++st, ++gs) {
           const uint32_t s = gs % NST;
           pf_wait(&full[s], (gs / NST) & 1u, status, &s_abort);
-          const uint64_t bdesc = umma_desc(smem_u32(sm + (size_t)s * STAGE + 2 * RAW_TILE), PF_BGRP, 128);
+          const uint32_t bbase = smem_u32(sm + (size_t)s * STAGE + 2 * RAW_TILE);
 #pragma unroll
           for (int j = 0; j < PF_SBK; ++j) {
             const bool ok = pf_wait(&a_full[slot], sph, status, &s_abort) &&
@@ -410,9 +409,10 @@ __global__ void __launch_bounds__(PF_THREADS, 1) pf_gemm(const __grid_constant__
             if (ok) {  // (aborted: the results are flagged invalid; issue nothing)
               tmem_fence_after();
               const uint32_t dc = taddr + slot * (2 * PF_NMAX), ac = taddr + PF_ACOL0 + slot * 32;
-              // B groups 4j, 4j+1 (K 0..15 of the block) and 4j+2, 4j+3 (K 16..31)
-              const uint64_t b0 = bdesc + (uint64_t)((4 * j) * PF_BGRP >> 4);
-              const uint64_t b1 = bdesc + (uint64_t)((4 * j + 2) * PF_BGRP >> 4);
+              // block j: chunk j / 2, bytes 64 (j % 2) .. +63 of each 128-byte row;
+              // K 0..15 of the block at +0, K 16..31 at +32
+              const uint32_t bj = bbase + (uint32_t)(j / 2) * PF_BCHUNK + (uint32_t)(j % 2) * 64;
+              const uint64_t b0 = umma_desc_sw128(bj), b1 = umma_desc_sw128(bj + 32);
               umma_f16_ts(dc, ac, b0, idesc, 0);
               umma_f16_ts(dc, ac + 8, b1, idesc, 1);
               umma_f16_ts(dc + PF_NMAX, ac + 16, b0, idesc, 0);
@@ -507,11 +507,13 @@ __global__ void __launch_bounds__(PF_THREADS, 1) pf_gemm(const __grid_constant__
       named_bar(1, 32 * PF_NEPI);  // every thread is done with the previous item's ring slots
 #pragma unroll 1
       for (int i = 0; i < PF_SCL; ++i) fetch(i);
-      float acc[2][PF_EPC];
+      // (column 2i, 2i + 1) pairs of each tile: one paired fp32 FMA per pair
+      // of block products, each result rounded once
+      float2 acc[2][PF_EPC / 2];
 #pragma unroll
       for (int tt = 0; tt < 2; ++tt)
 #pragma unroll
-        for (int j = 0; j < PF_EPC; ++j) acc[tt][j] = 0.f;
+        for (int j = 0; j < PF_EPC / 2; ++j) acc[tt][j] = make_float2(0.f, 0.f);
       const bool live = cg * PF_EPC < it.ntok;  // warp-uniform
       for (int st = 0; st < it.nst; ++st) {
         fetch(st + PF_SCL);
@@ -542,15 +544,16 @@ __global__ void __launch_bounds__(PF_THREADS, 1) pf_gemm(const __grid_constant__
               for (int i = 0; i < 4; ++i) sv[i] = s4[i];
 #pragma unroll
               for (int i = 0; i < 4; ++i) {
-                const int cc = h * 16 + 4 * i;
-                ffma2(acc[0][cc], acc[0][cc + 1], sv[i].x, sv[i].y, __uint_as_float(v0[4 * i]),
-                      __uint_as_float(v0[4 * i + 1]));
-                ffma2(acc[0][cc + 2], acc[0][cc + 3], sv[i].z, sv[i].w, __uint_as_float(v0[4 * i + 2]),
-                      __uint_as_float(v0[4 * i + 3]));
-                ffma2(acc[1][cc], acc[1][cc + 1], sv[i].x, sv[i].y, __uint_as_float(v1[4 * i]),
-                      __uint_as_float(v1[4 * i + 1]));
-                ffma2(acc[1][cc + 2], acc[1][cc + 3], sv[i].z, sv[i].w, __uint_as_float(v1[4 * i + 2]),
-                      __uint_as_float(v1[4 * i + 3]));
+                const int cp = (h * 16 + 4 * i) / 2;  // first column pair
+                const float2 s01 = make_float2(sv[i].x, sv[i].y), s23 = make_float2(sv[i].z, sv[i].w);
+                acc[0][cp] = __ffma2_rn(s01, make_float2(__uint_as_float(v0[4 * i]), __uint_as_float(v0[4 * i + 1])),
+                                        acc[0][cp]);
+                acc[0][cp + 1] = __ffma2_rn(
+                    s23, make_float2(__uint_as_float(v0[4 * i + 2]), __uint_as_float(v0[4 * i + 3])), acc[0][cp + 1]);
+                acc[1][cp] = __ffma2_rn(s01, make_float2(__uint_as_float(v1[4 * i]), __uint_as_float(v1[4 * i + 1])),
+                                        acc[1][cp]);
+                acc[1][cp + 1] = __ffma2_rn(
+                    s23, make_float2(__uint_as_float(v1[4 * i + 2]), __uint_as_float(v1[4 * i + 3])), acc[1][cp + 1]);
               }
               if (DUMP) {
                 const int bq = st * PF_SBK + j;
@@ -592,7 +595,9 @@ __global__ void __launch_bounds__(PF_THREADS, 1) pf_gemm(const __grid_constant__
         for (int j = 0; j < PF_EPC; ++j) {
           const int col = cg * PF_EPC + j;
           if (col >= it.ntok) continue;  // warp-uniform
-          const float gv = __fmul_rn(sg, acc[0][j]), uv = __fmul_rn(su, acc[1][j]);
+          const float ag = (j & 1) ? acc[0][j / 2].y : acc[0][j / 2].x;
+          const float au = (j & 1) ? acc[1][j / 2].y : acc[1][j / 2].x;
+          const float gv = __fmul_rn(sg, ag), uv = __fmul_rn(su, au);
           const float hv = __fmul_rn(__fdiv_rn(gv, 1.0f + expf(-gv)), uv);
           const bool bad = !isfinite(hv);
           const float hf = bad ? 0.f : hv;
@@ -617,7 +622,9 @@ __global__ void __launch_bounds__(PF_THREADS, 1) pf_gemm(const __grid_constant__
           const float sd = __ldg(sc + 2 * it.inter + row);
 #pragma unroll
           for (int j = 0; j < PF_EPC; ++j)
-            if (cg * PF_EPC + j < it.ntok) o[((size_t)it.pair0 + cg * PF_EPC + j) * H + row] = __fmul_rn(sd, acc[tt][j]);
+            if (cg * PF_EPC + j < it.ntok)
+              o[((size_t)it.pair0 + cg * PF_EPC + j) * H + row] =
+                  __fmul_rn(sd, (j & 1) ? acc[tt][j / 2].y : acc[tt][j / 2].x);
         }
       }
     }
@@ -677,16 +684,16 @@ cudaError_t launch_gemm(const PfMaps& maps, const PfParams& A, int grid, cudaStr
   return cudaGetLastError();
 }
 
-// fp16 codes [rows][k] in boxes of 8 codes x PF_NMAX rows
+// fp16 codes [rows][k] in boxes of 64 codes x PF_NMAX rows, 128-byte swizzle
 bool encode_codes(CUtensorMap* m, const void* base, int k, int rows) {
   auto fn = encode_fn();
   if (!fn || rows == 0) return false;
   const cuuint64_t dims[2] = {(cuuint64_t)k, (cuuint64_t)rows};
   const cuuint64_t strides[1] = {(cuuint64_t)k * 2};
-  const cuuint32_t box[2] = {8, PF_NMAX};
+  const cuuint32_t box[2] = {64, PF_NMAX};
   const cuuint32_t estr[2] = {1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<void*>(base), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
