@@ -311,7 +311,7 @@ int coli_moe_forward_dump(const coli_moe_cfg* cfg, const coli_moe_weights* weigh
  * library until the process exits).  It calls no cudaMalloc, cudaFree or
  * other allocating routine.  The caller still passes x, routing and y.
  *   - Limit: the layer's workspace for T positions must fit in
- *     COLI_STATIC_WS_BYTES (24 MiB: the GLM-5.2-shaped layer up to T = 88);
+ *     COLI_STATIC_WS_BYTES (24 MiB: the GLM-5.2-shaped layer up to T = 76);
  *     larger T returns COLI_EWORKSPACE and enqueues nothing.
  *   - The first call on a device looks up the array's device address
  *     (cudaGetSymbolAddress, with that device current) and caches it per
