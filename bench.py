@@ -256,11 +256,17 @@ class DecodeBench:
         return statistics.mean(d), statistics.median(d)
 
     def e2e_step(self, x_host, y_host):
-        """Public API per position with host buffers (copies inside)."""
+        """Public API per position with host buffers: each position's x is
+        copied in from pinned host memory before its own layer call and its y
+        copied out after it (a decode caller's per-token pattern)."""
         cm = self.cm
-        self.x.copy_(x_host, non_blocking=True)
-        self.step()
-        y_host.copy_(self.y, non_blocking=True)
+        for i in range(self.n):
+            r = i % self.R
+            rec = self.rep[r]
+            self.x[i:i + 1].copy_(x_host[i:i + 1], non_blocking=True)
+            cm.coli_moe_layer(self.cfg, self.W[r], self.x[i:i + 1], rec[4], rec[5], self.idx[i:i + 1],
+                              self.w[i:i + 1], self.y[i:i + 1], self.ws)
+            y_host[i:i + 1].copy_(self.y[i:i + 1], non_blocking=True)
         self.torch.cuda.synchronize()
 
 
@@ -377,7 +383,7 @@ def secondary(device, b):
     shape = b.shape
     # MTP verify: 4 correlated positions per call
     seed = synth.WORKLOADS["glm_mtp_verify_t4"][1]
-    calls = 100
+    calls = synth.WORKLOADS["glm_mtp_verify_t4"][3]   # 500 calls of 4 positions
     xs = np.stack([synth.mtp_chain(shape, seed, c) for c in range(calls)])
     x = torch.from_numpy(xs).to(device)
     wr = torch.from_numpy(synth.router_weight(shape, seed)).to(device)
@@ -439,6 +445,7 @@ def secondary(device, b):
     res["glm_gs64_mtp_verify_t4"] = weight_format_bench(device, b, calls=100, T=4)
     res["glm_int2_decode_b1"] = weight_format_bench(device, b, shape=synth.GLM_INT2)
     res["glm_int2_mtp_verify_t4"] = weight_format_bench(device, b, calls=100, T=4, shape=synth.GLM_INT2)
+    res["glm_prefill_sweep"] = prefill_sweep(device, b)
     res["glm_stack24_mtp1_b32"] = stack_bench(device, b)
     return res
 
@@ -503,6 +510,26 @@ def prefill_only(args):
     print(json.dumps({"workload": f"prefill: GLM-5.2-shaped layer with {shape.n_experts} routed experts, T={T}",
                       "ms_per_call": round(ms, 3), "tokens_per_s": round(T / (ms / 1e3), 1),
                       "status": cm.coli_moe_status(ws)}), flush=True)
+
+
+def sweep_only(args):
+    """--only sweep: the GLM-5.2-shaped layer at 64 .. 2048 positions per call
+    on one resident copy (the bench's prefill sweep alone)."""
+    import torch
+    import synth.gpu as sg
+    import quantized_expert_ffn_sigmoid_gb300 as cm
+    device = torch.device("cuda", 0)
+
+    class _B:  # the attributes prefill_sweep reads
+        pass
+    b = _B()
+    b.cm, b.shape, b.cfg = cm, synth.GLM, cm.Cfg.of(synth.GLM)
+    seed = synth.WORKLOADS["glm_prefill_s2048"][1]
+    recs, scs = sg.expert_records(synth.GLM, seed, 0, "routed", synth.GLM.n_experts, device)
+    srec, ssc = sg.expert_records(synth.GLM, seed, 0, "shared", 1, device)
+    b.W = [cm.make_weights(recs, scs, srec, ssc)]
+    print(json.dumps({"workload": "GLM-5.2-shaped layer, uniform routing, positions per call sweep",
+                      **prefill_sweep(device, b)}), flush=True)
 
 
 def few_only(args):
@@ -621,15 +648,19 @@ def weight_format_only(args, shape=synth.GLM_GS64, name="gs64", fmt="group-scale
               flush=True)
 
 
-def stack_bench(device, b, steps=4):
+def stack_bench(device, b, steps=None):
     """24 int4 GLM layers + 1 int8 layer resident, decode batch 32, Zipf-skewed
-    correction bias per layer, layer inputs x_{l+1} = x_l + delta_l (seeded,
-    independent of y_l); a step = the 25 layer calls, replayed from a graph."""
+    correction bias per layer.  A step is one coli_moe_stack_forward call: the
+    25 layers chained on the device (x_{l+1} = x_l + delta_l, the seeded
+    residual of every (step, layer), independent of y_l), replayed from one
+    CUDA graph whose input buffers are refilled from that step's seeded inputs
+    (the device-to-device refill is inside the timed region)."""
     import torch
     import synth.gpu as sg
     cm = b.cm
     seed = synth.WORKLOADS["glm_stack24_mtp1_b32"][1]
-    T, n_layers = 32, 25
+    steps = steps or synth.WORKLOADS["glm_stack24_mtp1_b32"][3]
+    T, n_layers, H = 32, 25, synth.GLM.hidden
     t0 = time.time()
     layers = []
     for l in range(n_layers):
@@ -641,62 +672,90 @@ def stack_bench(device, b, steps=4):
         layers.append((shape, cm.Cfg.of(shape), (recs, scs, srec, ssc), cm.make_weights(recs, scs, srec, ssc),
                        wr, bias))
     resident = sum(sum(a.numel() * a.element_size() for a in L[2]) for L in layers)
-    # layer inputs of every step: x_0 ~ N(0,1) per sequence, then the seeded residual adds
-    xs = torch.empty((steps, n_layers, T, synth.GLM.hidden), device=device)
+    # every step's inputs: x_0 ~ N(0,1) per sequence and the seeded residual of every layer
+    x0_all = torch.empty((steps, T, H), device=device)
+    res_all = torch.empty((steps, n_layers, T, H), device=device)
     for st in range(steps):
-        x = sg.token_batch(synth.GLM, seed, ("stack", st), range(T), device)
+        x0_all[st] = sg.token_batch(synth.GLM, seed, ("stack", st), range(T), device)
         for l in range(n_layers):
-            xs[st, l] = x
-            d = sg.normal_f32(synth.make_key(seed, "residual", st, l), 32 * synth.GLM.hidden, 0.1, device)
-            x = x + d[:T * synth.GLM.hidden].view(T, -1)
-    ws = cm.new_workspace(layers[0][1], T)
+            d = sg.normal_f32(synth.make_key(seed, "residual", st, l), 32 * H, 0.1, device)
+            res_all[st, l] = d[:T * H].view(T, H)
+    arr = cm.stack_layers([(L[1], L[3], L[4], L[5]) for L in layers])
+    xs = torch.empty((n_layers + 1, T, H), device=device)
+    res = torch.empty((n_layers, T, H), device=device)
     idx = torch.empty((n_layers, T, 8), dtype=torch.int32, device=device)
     w = torch.empty((n_layers, T, 8), device=device)
-    y = torch.empty((n_layers, T, synth.GLM.hidden), device=device)
+    y = torch.empty((n_layers, T, H), device=device)
+    ws = cm.new_workspace(max((L[1] for L in layers), key=lambda c: cm.coli_moe_workspace_size(c, T)), T)
     torch.cuda.synchronize()
-    log(f"[bench] stack: {resident / 1e9:.1f} GB resident in {time.time() - t0:.1f}s")
-    # unique experts per layer (for the bytes moved), from one pass of step 0
-    L = cm.coli_moe_workspace_layout(layers[0][1], T)
-    uniq = []
-    for l, (shape, cfg, _, W, wr, bias) in enumerate(layers):
-        cm.coli_moe_layer(cfg, W, xs[0, l], wr, bias, idx[l], w[l], y[l], ws)
-        uniq.append(int(ws[L.n_entries:L.n_entries + 4].view(torch.int32).item()) - shape.n_shared)
+    log(f"[bench] stack: {resident / 1e9:.1f} GB resident, {steps} steps of inputs in {time.time() - t0:.1f}s")
+    # unique experts per layer (for the bytes moved), from step 0
+    xs[0].copy_(x0_all[0])
+    res.copy_(res_all[0])
+    g = cm.capture_stack_step(arr, xs, res, idx, w, y, ws)
+    uniq = [int(torch.unique(idx[l]).numel()) for l in range(n_layers)]
+
     def ebytes(sh):
         return sh.record_bytes() + 4 * sh.scale_count()
     byt = sum((u + 1) * ebytes(synth.GLM_INT8 if l == 24 else synth.GLM) for l, u in enumerate(uniq)) \
         + n_layers * ROUTER_BYTES
 
     def one(st):
-        for l, (shape, cfg, _, W, wr, bias) in enumerate(layers):
-            cm.coli_moe_layer(cfg, W, xs[st, l], wr, bias, idx[l], w[l], y[l], ws)
-
-    graphs = []
-    for st in range(steps):
-        one(st)
-        torch.cuda.synchronize()
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, capture_error_mode="thread_local"):
-            one(st)
-        graphs.append(g)
-    for g in graphs:
+        xs[0].copy_(x0_all[st])
+        res.copy_(res_all[st])
         g.replay()
+    for st in range(min(3, steps)):
+        one(st)
     torch.cuda.synchronize()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record()
-    for g in graphs:
-        g.replay()
+    for st in range(steps):
+        one(st)
     e1.record()
     torch.cuda.synchronize()
     ms = e0.elapsed_time(e1) / steps
     st_code = cm.coli_moe_status(ws)
-    del layers, xs, ws
+    del layers, x0_all, res_all, ws
     torch.cuda.empty_cache()
     return {"tokens_per_s": round(T / (ms / 1e3), 1), "ms_per_step": round(ms, 3),
             "unique_experts_per_layer": round(sum(uniq) / n_layers, 1),
             "gbs": round(byt / (ms / 1e3) / 1e9, 1), "resident_gb": round(resident / 1e9, 1),
             "steps": steps, "status": st_code,
-            "note": "25 layer calls per step (24 int4 + 1 int8), step = 32 positions; bytes from step 0's unique experts"}
+            "note": "coli_moe_stack_forward (24 int4 + 1 int8 layers chained on the device) per step of 32 "
+                    "positions, one CUDA graph; input refill inside the timed region; bytes from step 0's "
+                    "unique experts"}
+
+
+def prefill_sweep(device, b, Ts=(64, 128, 256, 512, 1024, 2048)):
+    """The GLM-5.2-shaped layer on the tensor-core path at several call sizes
+    (uniform routing, every position's own experts): time per call, positions
+    per second, bytes of the distinct experts per second and int8-equivalent
+    operations per second."""
+    import torch
+    import synth.gpu as sg
+    cm = b.cm
+    shape = b.shape
+    seed = synth.WORKLOADS["glm_prefill_s2048"][1]
+    wr = torch.from_numpy(synth.router_weight(shape, seed)).to(device)
+    bias = torch.from_numpy(synth.zero_router_bias(shape)).to(device)
+    xall = sg.token_batch(shape, seed, 0, range(max(Ts)), device)
+    out = {}
+    for T in Ts:
+        x = xall[:T]
+        ws = cm.new_workspace(b.cfg, T)
+        idx = torch.empty((T, 8), dtype=torch.int32, device=device)
+        w = torch.empty((T, 8), dtype=torch.float32, device=device)
+        y = torch.empty((T, shape.hidden), dtype=torch.float32, device=device)
+        ms = time_graph(lambda: cm.coli_moe_layer(b.cfg, b.W[0], x, wr, bias, idx, w, y, ws), 3)
+        uniq = int(torch.unique(idx).numel())
+        byt = (uniq + 1) * EXPERT_BYTES + ROUTER_BYTES
+        ops = 2.0 * (T * 8 + T) * 3 * shape.inter * shape.hidden
+        out[str(T)] = {"ms_per_call": round(ms, 4), "tokens_per_s": round(T / (ms / 1e3), 1),
+                       "unique_experts": uniq, "gbs_min_bytes": round(byt / (ms / 1e3) / 1e9, 1),
+                       "int8_equiv_tops": round(ops / (ms / 1e3) / 1e12, 2), "status": cm.coli_moe_status(ws)}
+        del ws, idx, w, y
+    return out
 
 
 def time_graph(fn, reps):
@@ -738,15 +797,38 @@ def host_records(recs, scs, srec, ssc):
     return lambda kind, e: (R[e], S[e]) if kind == "routed" else (SR[e], SS[e])
 
 
+def oracle_parallel_tokens_per_s(get_record, router_w, bias, xs, budget_s, threads):
+    """The oracle as it stands on ``threads`` host threads: independent
+    positions, one oracle layer call each, dealt to the threads in waves until
+    ``budget_s`` (numpy releases the GIL in its array work; BLAS itself runs
+    single-threaded)."""
+    import concurrent.futures as cf
+    import oracle
+    shape = synth.GLM
+    n = 0
+    t0 = time.perf_counter()
+    with cf.ThreadPoolExecutor(threads) as ex:
+        while n < len(xs) and time.perf_counter() - t0 < budget_s:
+            wave = range(n, min(n + threads, len(xs)))
+            list(ex.map(lambda i: oracle.moe_layer(shape, get_record, xs[i:i + 1], router_w, bias), wave))
+            n += len(wave)
+    return n, time.perf_counter() - t0
+
+
 def cpu_baseline(b, budget_s):
-    xs = b.x[:16].cpu().numpy()
+    """The oracle on the host cores: one thread (serial) and every core."""
+    cores = os.cpu_count() or 1
+    xs = b.x[:max(16, 4 * cores)].cpu().numpy()
     rep = b.rep[0]
     get_record = host_records(rep[0], rep[1], rep[2], rep[3])
     wr = rep[4].cpu().numpy()
     bias = rep[5].cpu().numpy()
-    n, s = oracle_tokens_per_s(get_record, wr, bias, xs, budget_s)
-    return {"value": round(n / s, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": f"{n} positions of the decode workload, one layer call each (numpy, 1 thread)"}
+    n1, s1 = oracle_tokens_per_s(get_record, wr, bias, xs, budget_s / 2)
+    nc, sc = oracle_parallel_tokens_per_s(get_record, wr, bias, xs, budget_s / 2, cores)
+    return {"value": round(nc / sc, 4), "unit": UNIT, "cores": cores, "kind": "oracle",
+            "serial_value": round(n1 / s1, 4), "serial_cores": 1,
+            "sample": f"{nc} positions of the decode workload on {cores} threads and {n1} on one thread, "
+                      f"one oracle layer call each (numpy)"}
 
 
 def run_reference(args):
@@ -759,7 +841,9 @@ def run_reference(args):
     seed = synth.WORKLOADS["glm_decode_b1"][1]
     wr = synth.router_weight(shape, seed)
     bias = synth.router_bias(shape, seed)
-    xs = synth.token_batch(shape, seed, ("bench", 0), range(args.warmup + args.steps))
+    cores = os.cpu_count() or 1
+    per_step = cores          # one position per host thread and step
+    xs = synth.token_batch(shape, seed, ("bench", 0), range((args.warmup + args.steps) * per_step))
     # the layer's records, made by the generator before any timing (on the
     # device twin when a GPU is present: 4.9 GB in seconds instead of minutes)
     try:
@@ -779,20 +863,22 @@ def run_reference(args):
         cache = {("routed", e): synth.expert_record(shape, seed, 0, "routed", e) for e in sorted(need)}
         cache[("shared", 0)] = synth.expert_record(shape, seed, 0, "shared", 0)
         get_record = lambda kind, e: cache[(kind, e)]
-    per_step = 1
+    def step(i):
+        oracle_parallel_tokens_per_s(get_record, wr, bias, xs[i * per_step:(i + 1) * per_step], 1e9, cores)
     for i in range(args.warmup):
-        oracle_tokens_per_s(get_record, wr, bias, xs[i:i + 1], 1e9)
+        step(i)
     t0 = time.perf_counter()
     for i in range(args.steps):
-        oracle_tokens_per_s(get_record, wr, bias, xs[args.warmup + i:args.warmup + i + 1], 1e9)
+        step(args.warmup + i)
     s = time.perf_counter() - t0
     value = args.steps * per_step / s
     out = {"metric": METRIC, "value": round(value, 4), "unit": UNIT, "n_gpus": world, "steps": args.steps,
            "warmup": args.warmup, "ms_per_step": round(1e3 * s / args.steps, 2), "higher_is_better": True,
            "scaling": "weak", "vs_baseline": None, "dtype": "int8", "data": "synthetic", "impl": "reference",
            "config": {"workload": WORKLOAD, "positions_per_step": per_step},
-           "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
-                            "sample": f"{per_step} position per step of the decode workload (numpy, 1 thread)"},
+           "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": cores, "kind": "oracle",
+                            "sample": f"{per_step} positions per step of the decode workload, one per host "
+                                      f"thread ({cores} threads, numpy)"},
            "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(out), flush=True)
 
@@ -808,7 +894,7 @@ def main():
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--no-secondary", dest="secondary", action="store_false")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
-    ap.add_argument("--only", choices=["prefill", "mtp", "b32", "gs64", "int2"], default=None,
+    ap.add_argument("--only", choices=["prefill", "mtp", "b32", "gs64", "int2", "sweep"], default=None,
                     help="time one secondary workload alone (profiling)")
     ap.add_argument("--calls", type=int, default=20, help="calls per step of --only mtp / b32")
     ap.add_argument("--prefill-experts", type=int, default=256)
@@ -829,6 +915,8 @@ def main():
         weight_format_only(args)
     elif args.only == "int2":
         weight_format_only(args, shape=synth.GLM_INT2, name="int2", fmt="packed int2 with per-row scales")
+    elif args.only == "sweep":
+        sweep_only(args)
     else:
         run_gpu(args)
 

@@ -22,9 +22,9 @@ cudaError_t launch_decode_routed(const ExpertParams& P, const float* x, const fl
                                  int32_t* topk_idx, float* topk_w, int n_sm, cudaStream_t st);
 bool gemv_fits(const coli_moe_cfg& c, const Layout& L);
 bool prefill_fits(const coli_moe_cfg& c, int T);
-cudaError_t launch_prefill(const ExpertParams& P, int T, int n_sm, cudaStream_t st, bool dump);
-bool sb_fits(const coli_moe_cfg& c, const Layout& L);
-cudaError_t launch_sb(const ExpertParams& P, int n_sm, cudaStream_t st, bool dump);
+cudaError_t launch_prefill(const ExpertParams& P, int T, int n_sm, cudaStream_t st, bool dump, bool mixed);
+bool sb_fits(const coli_moe_cfg& c, const Layout& L, bool with_tensor_path);
+cudaError_t launch_sb(const ExpertParams& P, int n_sm, cudaStream_t st, bool dump, int max_pairs);
 size_t experts_smem_bytes(const coli_moe_cfg& c, const Layout& L);
 }  // namespace colimoe
 
@@ -129,6 +129,7 @@ ExpertParams expert_params(const coli_moe_cfg& c, const coli_moe_weights* w, con
   P.L = L;
   P.dump_gu = dump_gu;
   P.dump_d = dump_d;
+  P.ep_mul = ep_mul(c);
   return P;
 }
 
@@ -142,10 +143,16 @@ int do_experts(const coli_moe_cfg& c, const coli_moe_weights* w, int T, const fl
     return rc_of(launch_decode(P, x, idx, x == nullptr, n_sm, st, dump_gu || dump_d));
   }
   if (fast_paths(c) && prefill_fits(c, T)) {
-    // many positions: the expert products on the tensor cores
+    // many positions: per entry, the experts with at least PF_MIN_PAIRS pairs
+    // (and the shared experts) on the tensor cores, the others through the
+    // small-batch kernels, then one combine of every pair's output
     const int n_sm = sm_count();
     if (n_sm <= 0) return COLI_ECUDA;
-    return rc_of(launch_prefill(P, T, n_sm, st, dump_gu || dump_d));
+    const bool dump = dump_gu || dump_d;
+    if (!sb_fits(c, L, true)) return rc_of(launch_prefill(P, T, n_sm, st, dump, false));
+    const int rc = rc_of(launch_prefill(P, T, n_sm, st, dump, true));
+    if (rc != COLI_OK) return rc;
+    return rc_of(launch_sb(P, n_sm, st, dump, PF_MIN_PAIRS - 1));
   }
   if (T <= GEMV_MAX_T && per_row(c) && gemv_fits(c, L)) {
     // a few positions: stream the weights through the two GEMV kernels
@@ -153,11 +160,11 @@ int do_experts(const coli_moe_cfg& c, const coli_moe_weights* w, int T, const fl
     if (n_sm <= 0) return COLI_ECUDA;
     return rc_of(launch_gemv(P, n_sm, st, dump_gu || dump_d));
   }
-  if (fast_paths(c) && sb_fits(c, L)) {
+  if (fast_paths(c) && sb_fits(c, L, false)) {
     // up to a few dozen positions: weight rows on lanes, K split over warps
     const int n_sm = sm_count();
     if (n_sm <= 0) return COLI_ECUDA;
-    return rc_of(launch_sb(P, n_sm, st, dump_gu || dump_d));
+    return rc_of(launch_sb(P, n_sm, st, dump_gu || dump_d, 0x7fffffff));
   }
   const size_t smem = experts_smem_bytes(c, L);
   int dev_smem = 0, dev = 0;

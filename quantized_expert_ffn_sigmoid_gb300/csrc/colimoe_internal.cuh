@@ -30,7 +30,9 @@ constexpr int GEMV_SPLITS = 8;  // K splits of the router GEMV (T <= 8)
 constexpr int ROUTE_GEMV_MAX_T = 8;
 constexpr int PREP_THREADS = 1024;
 constexpr int GEMV_MAX_T = 4;   // calls up to this many positions take the streaming GEMV path
-constexpr int PF_MIN_T = 64;    // calls with at least this many positions take the tcgen05 path
+constexpr int PF_MIN_T = 64;    // calls with at least this many positions use the tensor cores ...
+constexpr int PF_MIN_PAIRS = 12;  // ... for the entries with at least this many pairs; the others
+                                  // stream through the small-batch kernels in the same call
 
 constexpr uint32_t SPIN_LIMIT = 1u << 22;  // bounded waits (about a second or more)
 
@@ -41,6 +43,13 @@ __host__ __device__ inline int row_bytes(int k, int bits) { return bits == 4 ? k
 __host__ __device__ inline bool ep_owned(const coli_moe_cfg& c, int e) {
   return c.ep_size <= 1 || e % c.ep_size == c.ep_rank;
 }
+// floor(e / ep_size) as one multiply-high by ep_mul(c) (kernels address
+// records in their inner loops, where an integer division would cost ~20
+// instructions): exact for e < 1024 and ep_size <= 1024.
+__host__ __device__ inline uint64_t ep_mul(const coli_moe_cfg& c) {
+  return c.ep_size <= 1 ? (1ull << 32) : (1ull << 32) / (uint64_t)c.ep_size + 1ull;
+}
+__host__ __device__ inline int ep_local_mul(uint64_t mul, int e) { return (int)(((uint64_t)e * mul) >> 32); }
 __host__ __device__ inline int ep_local(const coli_moe_cfg& c, int e) { return c.ep_size <= 1 ? e : e / c.ep_size; }
 // routed records held by this shard
 __host__ __device__ inline int ep_records(const coli_moe_cfg& c) {
@@ -164,6 +173,7 @@ struct ExpertParams {
   Layout L;
   int32_t* dump_gu;  // optional [P][2][imax][H/32]
   int32_t* dump_d;   // optional [P][H][imax/32]
+  uint64_t ep_mul;   // ep_mul(cfg): local record of routed expert e = ep_local_mul(ep_mul, e)
 };
 
 struct PrepParams {

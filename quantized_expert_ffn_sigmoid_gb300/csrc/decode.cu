@@ -114,7 +114,7 @@ __device__ __forceinline__ const uint8_t* dec_record(const ExpertParams& P, int 
   const int H = c.hidden, bits = c.weight_bits;
   const bool routed = expert < c.n_experts;
   const int I = routed ? c.inter : c.shared_inter;
-  const int e = routed ? ep_local(c, expert) : expert - c.n_experts;
+  const int e = routed ? ep_local_mul(P.ep_mul, expert) : expert - c.n_experts;
   const size_t rec = (size_t)2 * I * row_bytes(H, bits) + (size_t)H * row_bytes(I, bits);
   const size_t nsc = GS ? (size_t)3 * I * (H / 64) : (size_t)2 * I + H;
   *inter = I;

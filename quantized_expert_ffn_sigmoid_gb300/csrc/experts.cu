@@ -143,7 +143,7 @@ __device__ __forceinline__ const uint8_t* entry_record(const ExpertParams& P, in
   if (expert < c.n_experts) {
     const size_t rec = (size_t)2 * c.inter * row_bytes(H, bits) + (size_t)H * row_bytes(c.inter, bits);
     *inter_out = c.inter;
-    const int e = ep_local(c, expert);
+    const int e = ep_local_mul(P.ep_mul, expert);
     *scales_out = P.expert_scales + (size_t)e * scale_count(c, c.inter);
     return P.experts + (size_t)e * rec;
   }

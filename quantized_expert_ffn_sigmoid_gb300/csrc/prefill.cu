@@ -270,7 +270,9 @@ __global__ void __launch_bounds__(256) pf_gather(uint8_t* __restrict__ ws, Layou
 //   warps 12-19 epilogue, one row of each tile and 32 pair columns per
 //               thread: per-block scaling into register sums, then the item's
 //               SwiGLU + Q8_0 of h (gate/up) or row-scaled outputs (down).
-template <int BITS, bool GU, bool DUMP>
+// MIXED: entries with fewer than PF_MIN_PAIRS pairs are left to the
+// small-batch kernels of the same call
+template <int BITS, bool GU, bool DUMP, bool MIXED>
 __global__ void __launch_bounds__(PF_THREADS, 1) pf_gemm(const __grid_constant__ PfMaps maps, const PfParams A) {
   const ExpertParams& P = A.P;
   const coli_moe_cfg& c = P.cfg;
@@ -307,7 +309,9 @@ __global__ void __launch_bounds__(PF_THREADS, 1) pf_gemm(const __grid_constant__
     for (int u = 0; u < n_ent; ++u) {
       s_pre[u] = run;
       const int inter = u < n_uniq ? c.inter : c.shared_inter;
-      run += ((GU ? inter : H / 2) / PF_M) * ((e_cnt[u] + PF_NMAX - 1) / PF_NMAX);
+      const int cnt = e_cnt[u];
+      const int mine = (!MIXED || cnt >= PF_MIN_PAIRS) ? (cnt + PF_NMAX - 1) / PF_NMAX : 0;  // pair tiles here
+      run += ((GU ? inter : H / 2) / PF_M) * mine;
     }
     s_pre[n_ent] = run;
     s_n_items = run;
@@ -356,7 +360,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1) pf_gemm(const __grid_constant__
     const int nt = local % ntn;
     it.ntok = min(PF_NMAX, cnt - nt * PF_NMAX);
     it.pair0 = e_off[lo] + nt * PF_NMAX;
-    it.rec = it.routed ? ep_local(c, e_exp[lo]) : e_exp[lo] - E;
+    it.rec = it.routed ? ep_local_mul(P.ep_mul, e_exp[lo]) : e_exp[lo] - E;
     it.nst = (GU ? H : it.inter) / PF_KS;
     return it;
   };
@@ -666,21 +670,21 @@ __global__ void __launch_bounds__(256) pf_combine(const uint8_t* __restrict__ ws
 
 // ---------------------------------------------------------------- host
 namespace {
-template <int BITS, bool GU, bool DUMP>
+template <int BITS, bool GU, bool DUMP, bool MIXED>
 cudaError_t launch_gemm(const PfMaps& maps, const PfParams& A, int grid, cudaStream_t st) {
   const size_t smem = pf_smem(BITS) + 1024;  // + alignment slack
-  cudaError_t e = cudaFuncSetAttribute(pf_gemm<BITS, GU, DUMP>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  cudaError_t e = cudaFuncSetAttribute(pf_gemm<BITS, GU, DUMP, MIXED>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   // the warpgroups' register split must fit in what the CTA is launched with
   // (setmaxnreg.inc would otherwise wait for registers that never come)
   cudaFuncAttributes fa{};
-  e = cudaFuncGetAttributes(&fa, pf_gemm<BITS, GU, DUMP>);
+  e = cudaFuncGetAttributes(&fa, pf_gemm<BITS, GU, DUMP, MIXED>);
   if (e != cudaSuccess) return e;
   const long long need = 128LL * PF_REG_CTL + 32LL * PF_NCONV * PF_REG_CONV + 32LL * PF_NEPI * PF_REG_EPI;
   if ((long long)fa.numRegs * PF_THREADS < need || fa.numRegs < PF_REG_CTL || fa.numRegs < PF_REG_CONV ||
       fa.numRegs > PF_REG_EPI || fa.maxThreadsPerBlock < PF_THREADS)
     return cudaErrorInvalidConfiguration;
-  pf_gemm<BITS, GU, DUMP><<<grid, PF_THREADS, smem, st>>>(maps, A);
+  pf_gemm<BITS, GU, DUMP, MIXED><<<grid, PF_THREADS, smem, st>>>(maps, A);
   return cudaGetLastError();
 }
 
@@ -698,7 +702,7 @@ bool encode_codes(CUtensorMap* m, const void* base, int k, int rows) {
 }
 
 template <int BITS>
-cudaError_t run_prefill(const ExpertParams& P, int T, int n_sm, cudaStream_t st, bool dump) {
+cudaError_t run_prefill(const ExpertParams& P, int T, int n_sm, cudaStream_t st, bool dump, bool mixed) {
   const coli_moe_cfg& c = P.cfg;
   const Layout& L = P.L;
   const int H = c.hidden, I = c.inter, Is = c.shared_inter, ns = c.n_shared;
@@ -720,10 +724,13 @@ cudaError_t run_prefill(const ExpertParams& P, int T, int n_sm, cudaStream_t st,
   pf_gather<<<L.P, 256, 0, st>>>(P.ws, L, H);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  e = dump ? launch_gemm<BITS, true, true>(gu, A, n_sm, st) : launch_gemm<BITS, true, false>(gu, A, n_sm, st);
+  e = mixed ? (dump ? launch_gemm<BITS, true, true, true>(gu, A, n_sm, st) : launch_gemm<BITS, true, false, true>(gu, A, n_sm, st))
+            : (dump ? launch_gemm<BITS, true, true, false>(gu, A, n_sm, st) : launch_gemm<BITS, true, false, false>(gu, A, n_sm, st));
   if (e != cudaSuccess) return e;
-  e = dump ? launch_gemm<BITS, false, true>(dn, A, n_sm, st) : launch_gemm<BITS, false, false>(dn, A, n_sm, st);
+  e = mixed ? (dump ? launch_gemm<BITS, false, true, true>(dn, A, n_sm, st) : launch_gemm<BITS, false, false, true>(dn, A, n_sm, st))
+            : (dump ? launch_gemm<BITS, false, true, false>(dn, A, n_sm, st) : launch_gemm<BITS, false, false, false>(dn, A, n_sm, st));
   if (e != cudaSuccess) return e;
+  if (mixed) return cudaSuccess;  // the small-batch kernels follow and combine
   const long long n4 = (long long)T * (H / 4);
   const int blocks = (int)((n4 + 255) / 256 < 8LL * n_sm ? (n4 + 255) / 256 : 8LL * n_sm);
   pf_combine<<<blocks, 256, 0, st>>>(P.ws, L, T, H, c.top_k, ns, P.topk_w, P.y);
@@ -742,8 +749,9 @@ bool prefill_fits(const coli_moe_cfg& c, int T) {
          c.n_experts + c.n_shared <= MAX_E + MAX_SHARED && pf_smem(c.weight_bits) + 1024 <= (size_t)optin;
 }
 
-cudaError_t launch_prefill(const ExpertParams& P, int T, int n_sm, cudaStream_t st, bool dump) {
-  return P.cfg.weight_bits == 4 ? run_prefill<4>(P, T, n_sm, st, dump) : run_prefill<8>(P, T, n_sm, st, dump);
+cudaError_t launch_prefill(const ExpertParams& P, int T, int n_sm, cudaStream_t st, bool dump, bool mixed) {
+  return P.cfg.weight_bits == 4 ? run_prefill<4>(P, T, n_sm, st, dump, mixed)
+                                : run_prefill<8>(P, T, n_sm, st, dump, mixed);
 }
 
 }  // namespace colimoe

@@ -50,6 +50,7 @@ struct SbArgs {
   int cap;   // positions per item
   int nst;   // staging stages
   int swb;   // width of a weight slab in bytes (128: swizzled boxes; 64: plain)
+  int max_pairs;  // entries with more pairs are left to another kernel
 };
 
 struct SbGeo {
@@ -244,7 +245,7 @@ __global__ void __launch_bounds__(SB_THREADS, 1) sb_gemm(const __grid_constant__
     for (int base = 0; base < n_ent; base += 32) {
       const int u = base + lane;
       int v = 0;
-      if (u < n_ent) {
+      if (u < n_ent && t_cnt[u] <= A.max_pairs) {
         const int ntg = (t_cnt[u] + cap - 1) / cap;
         const int inter = t_exp[u] < E ? c.inter : c.shared_inter;
         v = ntg * (GU ? inter / RA : H / SB_ROWS);
@@ -280,7 +281,7 @@ __global__ void __launch_bounds__(SB_THREADS, 1) sb_gemm(const __grid_constant__
     d.pair0 = t_off[lo] + tg * cap;
     const int e = t_exp[lo];
     d.shared = e >= E;
-    d.ex = d.shared ? e - E : ep_local(P.cfg, e);
+    d.ex = d.shared ? e - E : ep_local_mul(P.ep_mul, e);
     d.inter = d.shared ? c.shared_inter : c.inter;
     d.chunks = (GU ? H : d.inter) / ck;
     return d;
@@ -548,7 +549,7 @@ cudaError_t launch_one(const SbMaps& maps, const SbArgs& A, size_t smem, int gri
 }
 
 template <int BITS>
-cudaError_t run_sb(const ExpertParams& P, int n_sm, cudaStream_t st, bool dump) {
+cudaError_t run_sb(const ExpertParams& P, int n_sm, cudaStream_t st, bool dump, int max_pairs) {
   const coli_moe_cfg& c = P.cfg;
   const int H = c.hidden, E = c.n_experts, I = c.inter, Is = c.shared_inter, ns = c.n_shared;
   SbPlan pg, pd;
@@ -565,7 +566,7 @@ cudaError_t run_sb(const ExpertParams& P, int n_sm, cudaStream_t st, bool dump) 
     dn.w_sh = dn.w;
   }
   if (!ok) return cudaErrorInvalidValue;
-  const SbArgs ag{P, pg.ck, pg.cap, pg.nst, pg.swb}, ad{P, pd.ck, pd.cap, pd.nst, pd.swb};
+  const SbArgs ag{P, pg.ck, pg.cap, pg.nst, pg.swb, max_pairs}, ad{P, pd.ck, pd.cap, pd.nst, pd.swb, max_pairs};
   cudaError_t e = pg.cap <= 4 ? launch_one<BITS, true, 4>(gu, ag, pg.smem, n_sm, st, dump)
                               : launch_one<BITS, true, 8>(gu, ag, pg.smem, n_sm, st, dump);
   if (e != cudaSuccess) return e;
@@ -588,14 +589,14 @@ cudaError_t run_sb(const ExpertParams& P, int n_sm, cudaStream_t st, bool dump) 
 
 }  // namespace
 
-bool sb_fits(const coli_moe_cfg& c, const Layout& L) {
-  if (L.T < 2 || L.T >= PF_MIN_T || !encode_fn()) return false;
+bool sb_fits(const coli_moe_cfg& c, const Layout& L, bool with_tensor_path) {
+  if (L.T < 2 || (!with_tensor_path && L.T >= PF_MIN_T) || !encode_fn()) return false;
   SbPlan p;
   return sb_plan(c, L, true, &p) && sb_plan(c, L, false, &p);
 }
 
-cudaError_t launch_sb(const ExpertParams& P, int n_sm, cudaStream_t st, bool dump) {
-  return P.cfg.weight_bits == 4 ? run_sb<4>(P, n_sm, st, dump) : run_sb<8>(P, n_sm, st, dump);
+cudaError_t launch_sb(const ExpertParams& P, int n_sm, cudaStream_t st, bool dump, int max_pairs) {
+  return P.cfg.weight_bits == 4 ? run_sb<4>(P, n_sm, st, dump, max_pairs) : run_sb<8>(P, n_sm, st, dump, max_pairs);
 }
 
 }  // namespace colimoe

@@ -175,6 +175,7 @@ def check_parity(layer: DeviceLayer, x, g, ref=None, idx=None, w=None, tokens=No
     stats = dict(qh_checked=0, qh_unstable=0, qh_flips=0, accd_blocks=0, pairs=0)
     y_delta = np.zeros((sel.size, H))   # linear effect of the GPU's admissible qh steps
     bound = np.zeros((sel.size, H))     # elementwise bound on |y_gpu - y_oracle|
+    stepped = np.zeros(sel.size, bool)  # positions with an admissible qh step in any of their pairs
     gsz = shape.group_size
 
     def on_entry(kind, e, pr):
@@ -231,6 +232,7 @@ def check_parity(layer: DeviceLayer, x, g, ref=None, idx=None, w=None, tokens=No
         # combine rounding (fp32, k + n_shared terms) and fp32 gate weights
         bnd = np.abs(wt)[:, None] * (term + np.abs(pr["o"]) * (2.0 ** -20 + 2e-6))
         with lock:
+            stepped[tl[(qh_g != qh_r).any(axis=1)]] = True
             np.add.at(y_delta, tl, wt[:, None] * adj)
             np.add.at(bound, tl, bnd)
             stats["qh_checked"] += qh_g.size
@@ -247,13 +249,18 @@ def check_parity(layer: DeviceLayer, x, g, ref=None, idx=None, w=None, tokens=No
     err = normwise_err(y_g, ref["y"] + y_delta)
     assert err <= Y_TOL, f"layer output error {err:.3e} (against the oracle for the GPU's h codes)"
     stats["y_err"] = err
-    # against the oracle's own output: the 1e-3 bound holds for int4 and int8
-    # weights; with packed int2 one admissible h step can move y by more
-    # than that, so there only the adjusted comparison above is asserted
+    # against the oracle's own output: asserted for every position whose h
+    # codes all equal the oracle's.  Where the GPU's fp32 h fell on the other
+    # side of a Q8_0 rounding boundary (both codes are quantisations of h
+    # within its fp32 error; checked above to be exactly such steps), one
+    # code step can move y by more than 1e-3 of max|y| on narrow layers; those
+    # positions are held to the adjusted bound and the elementwise bound.
     stats["y_err_unadjusted"] = normwise_err(y_g, ref["y"])
-    if shape.weight_bits != 2:
-        assert stats["y_err_unadjusted"] <= Y_TOL, \
-            f"layer output error {stats['y_err_unadjusted']:.3e} against the oracle's own output"
+    stats["positions_with_h_step"] = int(stepped.sum())
+    clean = ~stepped
+    stats["y_err_unadjusted_no_step"] = normwise_err(y_g[clean], ref["y"][clean])
+    assert stats["y_err_unadjusted_no_step"] <= Y_TOL, \
+        f"layer output error {stats['y_err_unadjusted_no_step']:.3e} against the oracle's own output"
     stats["y_err_elementwise_rms_floor"] = elementwise_err(y_g, ref["y"])
     dy = np.abs(y_g.astype(np.float64) - ref["y"])
     assert np.all(dy <= bound + 1e-30), f"elementwise output bound exceeded by {(dy - bound).max():.3e}"

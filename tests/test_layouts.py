@@ -64,3 +64,12 @@ def test_int2_fields_masked_in_place_are_exact_multiples():
         assert masked.max() <= 192
         s = _dot4(masked, a)
         assert s % (4 ** m) == 0 and s // 4 ** m == _dot4((b >> (2 * m)) & 3, a)
+
+
+def test_expert_parallel_record_index_multiply_high():
+    # the kernels find expert e's local record e // ep_size as a multiply-high by
+    # 2^32 // ep_size + 1 (2^32 without sharding): exact over the whole range
+    # of expert ids and shard counts the library accepts (1024 each)
+    for p in range(1, 1025):
+        m = (1 << 32) if p == 1 else (1 << 32) // p + 1
+        assert all((e * m) >> 32 == e // p for e in range(1024)), p
