@@ -151,7 +151,7 @@ size_t coli_moe_workspace_size(const coli_moe_cfg* cfg, int32_t max_T);
 
 /* Clears the header of a workspace (enqueued on `stream`): the status word,
  * the device counters and the router's tagged exchange words, i.e. the first
- * min(ws_bytes, 8448) bytes. */
+ * min(ws_bytes, 8704) bytes. */
 int coli_moe_workspace_init(void* ws, size_t ws_bytes, cudaStream_t stream);
 
 /* Router: "How it works (validated core mechanics)" on the page-4 write-up

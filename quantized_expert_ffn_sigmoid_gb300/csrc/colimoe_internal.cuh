@@ -25,7 +25,8 @@ constexpr int MAX_SHARED = 8;
 constexpr int MAX_GROUPS = 32;
 // bytes at the start of a workspace that coli_moe_workspace_init clears:
 // status and counter words, then the router's tagged exchange words
-constexpr size_t WS_HEADER_BYTES = 256 + 8 * (size_t)MAX_E;
+constexpr size_t WS_STATUS_BYTES = 512;  // status word and device counters (128 words)
+constexpr size_t WS_HEADER_BYTES = WS_STATUS_BYTES + 8 * (size_t)MAX_E;
 constexpr int GEMV_SPLITS = 8;  // K splits of the router GEMV (T <= 8)
 constexpr int ROUTE_GEMV_MAX_T = 8;
 constexpr int PREP_THREADS = 1024;
@@ -109,7 +110,7 @@ __host__ __device__ inline Layout make_layout(const coli_moe_cfg& c, int T) {
   L.imax = c.inter > c.shared_inter ? c.inter : c.shared_inter;
   size_t off = 0;
   auto take = [&](size_t bytes) { size_t r = off; off = align_up(off + bytes, 256); return r; };
-  L.status = take(256);
+  L.status = take(WS_STATUS_BYTES);
   L.route_words = take(8 * (size_t)MAX_E);  // zeroed by coli_moe_workspace_init with the status words
   L.counters = take(4 * (1 + L.n_ent_max + L.n_tiles));
   L.hdr = take(4 * H_FIELDS);
@@ -273,9 +274,25 @@ __device__ __forceinline__ uint64_t ld_relaxed_u64(const uint64_t* p) {
 __device__ __forceinline__ void st_relaxed_u64(uint64_t* p, uint64_t v) {
   asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }
+__device__ __forceinline__ void red_relaxed_add(uint32_t* p, uint32_t v) {
+  asm volatile("red.relaxed.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
 __device__ __forceinline__ void red_release_add(uint32_t* p, uint32_t v) {
   asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
+__device__ __forceinline__ uint32_t ld_acquire_shared_u32(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.cta.shared::cta.u32 %0, [%1];" : "=r"(v) : "r"(smem_u32(p)) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_release_shared_u32(uint32_t* p, uint32_t v) {
+  asm volatile("st.release.cta.shared::cta.u32 [%0], %1;" ::"r"(smem_u32(p)), "r"(v) : "memory");
+}
+// 16 bytes global -> shared through L2 only (both 16-byte aligned)
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 __device__ __forceinline__ uint32_t atom_acq_rel_add(uint32_t* p, uint32_t v) {
   uint32_t old;
   asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");

@@ -53,8 +53,10 @@ extern "C" int coli_moe_forward_static(const coli_moe_cfg* cfg, const coli_moe_w
   void* ws = nullptr;
   const int rc = static_ws_ptr(&ws);
   if (rc != COLI_OK) return rc;
-  // The tables, counters and intermediates that coli_moe_forward keeps in its
-  // workspace are all rewritten (counters re-zeroed) by every call, so the
-  // previous call's contents never leak into the next one.
+  // The tables and intermediates that coli_moe_forward keeps in its
+  // workspace are rewritten by every call, and the fused single-position
+  // kernel's counters come in two sets that each call clears for the next
+  // one, so the previous call's contents never leak into the next one (the
+  // scratch starts zeroed, like a workspace after coli_moe_workspace_init).
   return coli_moe_forward(cfg, weights, x, T, topk_idx, topk_w, y, ws, (size_t)COLI_STATIC_WS_BYTES, stream);
 }
