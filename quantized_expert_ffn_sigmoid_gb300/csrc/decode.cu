@@ -237,6 +237,13 @@ decode_layer_kernel(ExpertParams P, const float* __restrict__ x, const int32_t* 
   __syncthreads();
 
   // ---------------------------------------------------------- before the dependency wait: weights only
+  // In the routing mode a CTA whose first item is a shared-expert tile (known
+  // without the routing) requests that tile's rows now and computes its h
+  // while the routing completes (its requantisation waits for the pair
+  // tables).  Not with group scales: their scale slots share the area the
+  // router's scratch uses.
+  const bool early = MODE == DM_ROUTE && !GS && (int)blockIdx.x < n_sh_items;
+  if (early && lane == 0) top_up(0, DK_RPW);
   // router task of this warp: expert blockIdx.x * epc + warp / splits, K split warp % splits
   const int rsplits = MODE == DM_ROUTE ? R.splits : 1;
   const int rn4 = H / 4 / rsplits;
@@ -278,7 +285,7 @@ decode_layer_kernel(ExpertParams P, const float* __restrict__ x, const int32_t* 
   }
 
   // ---------------------------------------------------------- router partial logits
-  uint64_t early = 0;  // first probe of this thread's logit word, read back after the Q8_0 pass
+  uint64_t lprobe = 0;  // first probe of this thread's logit word, read back after the Q8_0 pass
   if (MODE == DM_ROUTE) {
     if (r_task) {
       const float4* x4 = reinterpret_cast<const float4*>(x) + (size_t)(warp % rsplits) * rn4;
@@ -309,7 +316,7 @@ decode_layer_kernel(ExpertParams P, const float* __restrict__ x, const int32_t* 
     // this CTA's shared tile (its first item) into L2 while the routing
     // completes: no shared-memory slot is held, so the routed tiles' copies
     // are not held up behind it (each warp: two consecutive gate and up rows)
-    if ((int)blockIdx.x < n_sh_items && lane == 0) {
+    if (!early && (int)blockIdx.x < n_sh_items && lane == 0) {
       const int it = blockIdx.x;
       int inter;
       const float* sc;
@@ -318,7 +325,7 @@ decode_layer_kernel(ExpertParams P, const float* __restrict__ x, const int32_t* 
       prefetch_l2(rec + (size_t)row * rb, (uint32_t)(DK_RPW * rb));
       prefetch_l2(rec + (size_t)(inter + row) * rb, (uint32_t)(DK_RPW * rb));
     }
-    if (tid < E) early = ld_relaxed_u64(rwords + tid);
+    if (tid < E) lprobe = ld_relaxed_u64(rwords + tid);
   }
 
   // ---------------------------------------------------------- Q8_0 of x
@@ -499,13 +506,15 @@ decode_layer_kernel(ExpertParams P, const float* __restrict__ x, const int32_t* 
     if (lane == 0) red_release_add(ent_done + u, 1u);
   };
 
+  if (early) gu_item(0, DK_RPW);
+
   // ---------------------------------------------------------- routing
   if (MODE == DM_ROUTE) {
     // every expert's logit word, once it carries this call's tag (bounded wait)
     float* s_logit = reinterpret_cast<float*>(dact);
     const uint32_t tag = s_epoch + 1u;
     for (int e = tid; e < E; e += DK_THREADS) {
-      uint64_t v = e == tid ? early : 0;
+      uint64_t v = e == tid ? lprobe : 0;
       bool ok = e == tid && (uint32_t)(v >> 32) == tag;
       for (uint32_t i = 0; i < SPIN_LIMIT && !ok; ++i) {
         v = ld_relaxed_u64(rwords + e);
@@ -749,11 +758,13 @@ decode_layer_kernel(ExpertParams P, const float* __restrict__ x, const int32_t* 
   // ---------------------------------------------------------- phase 1: gate / up
   const int nmine = nA > (int)blockIdx.x ? (nA - 1 - (int)blockIdx.x) / G + 1 : 0;
   const int total = nmine * DK_RPW;
-  if (lane == 0) top_up(0, total);
+  const int j0 = early ? 1 : 0;   // items done before the routing
+  if (lane == 0) top_up(j0 * DK_RPW, total);
   // per-row down scales (shared-memory region idle in phase 1 without group
   // scales), read while the first gate/up rows are in flight
   if (!GS && ngr > 0) load_scales(g0);
-  for (int j = 0; j < nmine; ++j) {
+  if (early) requant_item(0);
+  for (int j = j0; j < nmine; ++j) {
     gu_item(j, total);
     if (j > 0) count_item(j - 1);
     requant_item(j);
