@@ -445,6 +445,7 @@ def secondary(device, b):
     res["glm_gs64_mtp_verify_t4"] = weight_format_bench(device, b, calls=100, T=4)
     res["glm_int2_decode_b1"] = weight_format_bench(device, b, shape=synth.GLM_INT2)
     res["glm_int2_mtp_verify_t4"] = weight_format_bench(device, b, calls=100, T=4, shape=synth.GLM_INT2)
+    res["glm_int2_b32"] = weight_format_bench(device, b, calls=20, T=32, shape=synth.GLM_INT2)
     res["glm_prefill_sweep"] = prefill_sweep(device, b)
     res["glm_stack24_mtp1_b32"] = stack_bench(device, b)
     return res
@@ -599,6 +600,8 @@ def weight_format_bench(device, b, calls=300, T=1, shape=synth.GLM_GS64):
     Ws = [cm.make_weights(r[0], r[1], r[2], r[3]) for r in reps]
     if T == 1:
         x = sg.token_batch(shape, seed, ("gs64", 0), range(calls), device).view(calls, 1, -1)
+    elif T > 4:  # a decode batch: T independent positions per call
+        x = sg.token_batch(shape, seed, ("batch", T), range(calls * T), device).view(calls, T, -1)
     else:  # the MTP-verify chain: T correlated positions per call
         mseed = synth.WORKLOADS["glm_mtp_verify_t4"][1]
         x = torch.from_numpy(np.stack([synth.mtp_chain(shape, mseed, c, n_pos=T) for c in range(calls)])).to(device)
@@ -626,6 +629,7 @@ def weight_format_bench(device, b, calls=300, T=1, shape=synth.GLM_GS64):
            "note": (("packed int2, per-row scales" if shape.weight_bits == 2 else "group-scaled int4 (gs64)") +
                     (", the fused single-position kernel" if T == 1 else
                      ", the few-position kernels" if shape.weight_bits == 2 and T <= 4 else
+                     ", the small-batch kernels" if shape.weight_bits == 2 else
                      ", the general expert kernel") +
                     f", {T} position(s) per call; 8 rotated copies")}
     del reps, Ws, recs, scs, srec, ssc
@@ -641,10 +645,10 @@ def weight_format_only(args, shape=synth.GLM_GS64, name="gs64", fmt="group-scale
     class _B:  # the two attributes weight_format_bench reads
         import quantized_expert_ffn_sigmoid_gb300 as cm
         R = REPLICAS
-    for T in (1, 4):
+    for T in (1, 4, 32):
         print(json.dumps({"workload": f"{name}: GLM-5.2-shaped layer, {fmt}, {T} position(s) per call",
-                          **weight_format_bench(torch.device("cuda", 0), _B, calls=300 if T == 1 else 100, T=T,
-                                       shape=shape)}),
+                          **weight_format_bench(torch.device("cuda", 0), _B,
+                                                calls=300 if T == 1 else 100 if T == 4 else 20, T=T, shape=shape)}),
               flush=True)
 
 

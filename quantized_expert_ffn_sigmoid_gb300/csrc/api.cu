@@ -23,7 +23,7 @@ cudaError_t launch_decode_routed(const ExpertParams& P, const float* x, const fl
 bool gemv_fits(const coli_moe_cfg& c, const Layout& L);
 bool prefill_fits(const coli_moe_cfg& c, int T);
 cudaError_t launch_prefill(const ExpertParams& P, int T, int n_sm, cudaStream_t st, bool dump, bool mixed);
-bool sb_fits(const coli_moe_cfg& c, const Layout& L, bool with_tensor_path);
+bool sb_fits(const coli_moe_cfg& c, const Layout& L, bool large_T_ok);
 cudaError_t launch_sb(const ExpertParams& P, int n_sm, cudaStream_t st, bool dump, int max_pairs);
 size_t experts_smem_bytes(const coli_moe_cfg& c, const Layout& L);
 }  // namespace colimoe
@@ -66,7 +66,8 @@ int check_cfg(const coli_moe_cfg* c) {
 // scale layouts) or else on the general expert kernel, and packed int2
 // beyond the few-position sizes on the general expert kernel.
 bool per_row(const coli_moe_cfg& c) { return c.group_size == 0; }
-bool fast_paths(const coli_moe_cfg& c) { return per_row(c) && c.weight_bits != 2; }
+// per-row scales: the few-position, small-batch and (int4 / int8) tensor-core kernels
+bool fast_paths(const coli_moe_cfg& c) { return per_row(c); }
 
 coli_moe_cfg normalized(const coli_moe_cfg* c) {
   coli_moe_cfg n = *c;
@@ -160,8 +161,9 @@ int do_experts(const coli_moe_cfg& c, const coli_moe_weights* w, int T, const fl
     if (n_sm <= 0) return COLI_ECUDA;
     return rc_of(launch_gemv(P, n_sm, st, dump_gu || dump_d));
   }
-  if (fast_paths(c) && sb_fits(c, L, false)) {
-    // up to a few dozen positions: weight rows on lanes, K split over warps
+  if (fast_paths(c) && sb_fits(c, L, c.weight_bits == 2)) {
+    // up to a few dozen positions (packed int2: any number, the tensor-core
+    // path takes int4 and int8 only): weight rows on lanes, K split over warps
     const int n_sm = sm_count();
     if (n_sm <= 0) return COLI_ECUDA;
     return rc_of(launch_sb(P, n_sm, st, dump_gu || dump_d, 0x7fffffff));

@@ -102,6 +102,16 @@ def test_glm_int2_parity(glm2, T):
     print("int2 T", T, st)
 
 
+@pytest.mark.parametrize("T", [32, 70])
+def test_glm_int2_small_batch(glm2, T):
+    """Packed int2 on the small-batch kernels (more than four positions, also
+    beyond the tensor-core path's lower bound, which takes int4 and int8
+    only): every table, code and output against the oracle."""
+    x, _, _ = margin_batch(glm2.shape, glm2.seed, ("glm_int2_sb", T), T, glm2.router_w, glm2.bias)
+    st = check_parity(glm2, x, glm2.run(x, dump=False))
+    print("int2 small batch T", T, st)
+
+
 def test_glm_int2_fused_decode(glm2):
     """One fused launch per position (router inside) on packed int2 experts,
     two calls in a row on one workspace; the split calls give the same y."""
