@@ -446,6 +446,7 @@ def secondary(device, b):
     res["glm_int2_decode_b1"] = weight_format_bench(device, b, shape=synth.GLM_INT2)
     res["glm_int2_mtp_verify_t4"] = weight_format_bench(device, b, calls=100, T=4, shape=synth.GLM_INT2)
     res["glm_int2_b32"] = weight_format_bench(device, b, calls=20, T=32, shape=synth.GLM_INT2)
+    res["glm_gs64_b32"] = weight_format_bench(device, b, calls=20, T=32)
     res["glm_prefill_sweep"] = prefill_sweep(device, b)
     res["glm_stack24_mtp1_b32"] = stack_bench(device, b)
     return res
@@ -629,8 +630,7 @@ def weight_format_bench(device, b, calls=300, T=1, shape=synth.GLM_GS64):
            "note": (("packed int2, per-row scales" if shape.weight_bits == 2 else "group-scaled int4 (gs64)") +
                     (", the fused single-position kernel" if T == 1 else
                      ", the few-position kernels" if shape.weight_bits == 2 and T <= 4 else
-                     ", the small-batch kernels" if shape.weight_bits == 2 else
-                     ", the general expert kernel") +
+                     ", the small-batch kernels") +
                     f", {T} position(s) per call; 8 rotated copies")}
     del reps, Ws, recs, scs, srec, ssc
     torch.cuda.empty_cache()

@@ -161,9 +161,10 @@ int do_experts(const coli_moe_cfg& c, const coli_moe_weights* w, int T, const fl
     if (n_sm <= 0) return COLI_ECUDA;
     return rc_of(launch_gemv(P, n_sm, st, dump_gu || dump_d));
   }
-  if (fast_paths(c) && sb_fits(c, L, c.weight_bits == 2)) {
-    // up to a few dozen positions (packed int2: any number, the tensor-core
-    // path takes int4 and int8 only): weight rows on lanes, K split over warps
+  if (sb_fits(c, L, c.weight_bits == 2 || c.group_size != 0)) {
+    // up to a few dozen positions (packed int2 and group-scaled int4: any
+    // number, the tensor-core path takes per-row int4 and int8 only): weight
+    // rows on lanes, K split over warps
     const int n_sm = sm_count();
     if (n_sm <= 0) return COLI_ECUDA;
     return rc_of(launch_sb(P, n_sm, st, dump_gu || dump_d, 0x7fffffff));

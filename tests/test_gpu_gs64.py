@@ -69,6 +69,28 @@ def test_glm_gs64_parity(glm_gs, T):
     print("gs64 T", T, st)
 
 
+@pytest.mark.parametrize("T", [32, 70])
+def test_glm_gs64_small_batch(glm_gs, T):
+    """Group-scaled int4 on the small-batch kernels (every row's group scales
+    of a K chunk staged beside its weights), also beyond the tensor-core
+    path's lower bound (that path takes per-row scales only)."""
+    x, _, _ = margin_batch(glm_gs.shape, glm_gs.seed, ("glm_gs64_sb", T), T, glm_gs.router_w, glm_gs.bias)
+    st = check_parity(glm_gs, x, glm_gs.run(x, dump=False))
+    print("gs64 small batch T", T, st)
+
+
+@pytest.mark.parametrize("T", [2, 4, 9, 40])
+def test_gs64_small_batch_block_dots(T):
+    """A small layer whose K lengths (256) let the small-batch kernels take
+    group scales: every int32 gate, up and down block dot dumped and compared
+    bit for bit, outputs within 1e-3; a shared expert of another size."""
+    import dataclasses
+    shape = dataclasses.replace(synth.TINY_GS64, inter=256, shared_inter=512)
+    L = DeviceLayer(shape, 12)
+    x, _, _ = margin_batch(shape, 12, ("gs64sb", T), T, L.router_w, L.bias)
+    check_parity(L, x, L.run(x))
+
+
 def test_glm_gs64_fused_decode(glm_gs):
     """One fused launch per position (router inside) on group-scaled experts."""
     ws = cm.new_workspace(glm_gs.cfg, 1)
