@@ -154,7 +154,8 @@ size_t coli_moe_workspace_size(const coli_moe_cfg* cfg, int32_t max_T);
  * min(ws_bytes, 8704) bytes. */
 int coli_moe_workspace_init(void* ws, size_t ws_bytes, cudaStream_t stream);
 
-/* Router: "How it works (validated core mechanics)" on the page-4 write-up
+/* Router: "How it works (validated core mechanics)" of the GLM-5.2 write-up
+ * ("Colibri (colibrì): GLM-5.2 local inference on 25 GB of RAM")
  * (sigmoid affinities, bias for ranking only, lower id wins ties, unbiased
  * renormalised weights, non-finite input rejected) with DeepSeek-V3 group
  * limiting: group score = sum of the two best biased scores of the group,

@@ -18,7 +18,7 @@ It computes the layer literally, following the colibrì pages:
   "What's implemented" (integer-dot kernels, quantization kernels,
   batch-union MoE) and "Experimental Metal backend" (routed-expert SwiGLU).
 * the routing-weighted combine plus the always-on shared expert -- the
-  router description on the page-4 write-up and "What's implemented".
+  router description on the GLM-5.2 write-up ("Colibri (colibrì): GLM-5.2 local inference on 25 GB of RAM") and "What's implemented".
 
 Floating point is fp64 except where a floating-point value decides an
 integer code (the Q8_0 scale and rounding), which is done in fp32 exactly as

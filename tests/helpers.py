@@ -74,7 +74,7 @@ def elementwise_err(y_gpu, y_ref, floor=1e-3):
 
 
 # ------------------------------------------------------------- exact ties
-# The page-4 write-up's router check ("How it works (validated core
+# The GLM-5.2 write-up's router check ("How it works (validated core
 # mechanics)") sends an exact tie to the lower expert id; the same rule is
 # taken for group ties.  With zero router rows every logit is 0 and every
 # affinity sigmoid(0) = 1/2 exactly, and a bias on a 2^-10 grid keeps every

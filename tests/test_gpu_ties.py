@@ -1,6 +1,6 @@
 """Exact router ties on the GPU, checked bit for bit against the oracle.
 
-The page-4 write-up ("Colibri (colibrì): GLM-5.2 local inference on 25 GB of
+The GLM-5.2 write-up ("Colibri (colibrì): GLM-5.2 local inference on 25 GB of
 RAM", "How it works (validated core mechanics)") sends an exact tie to the
 lower expert id; group ties follow the same rule.  Two constructions make
 the ties exact on both sides:

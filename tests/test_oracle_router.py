@@ -1,4 +1,4 @@
-"""Pins for the oracle's router: the page-4 router check re-run as data,
+"""Pins for the oracle's router: the GLM-5.2 write-up's router check re-run as data,
 brute-force enumeration of group and expert subsets, closed forms."""
 import itertools
 import json
@@ -19,8 +19,8 @@ def cfg(G, tg, k, rsf=1.0):
     return SimpleNamespace(n_groups=G, topk_group=tg, top_k=k, routed_scaling_factor=rsf)
 
 
-def test_page4_router_cases():
-    gold = json.load(open(os.path.join(GOLD, "router_page4_cases.json")))
+def test_writeup_router_cases():
+    gold = json.load(open(os.path.join(GOLD, "router_glm52_writeup_cases.json")))
     for c in gold["cases"]:
         idx, w = oracle.route(np.array([c["logits"]]), np.array(c["bias"], np.float32),
                               cfg(1, 1, c["top_k"]))
@@ -74,7 +74,7 @@ def test_route_matches_brute_force(E, G, tg, k):
 
 
 def test_single_group_is_plain_topk():
-    # with one group the router is the plain sigmoid top-k of the page-4 check:
+    # with one group the router is the plain sigmoid top-k of the write-up's check:
     # full order by (-score, id)
     rng = np.random.default_rng(7)
     logits = rng.normal(size=(64, 256))
@@ -147,7 +147,7 @@ def test_config_validation():
 
 def test_designed_exact_ties_select_as_derived_by_hand():
     """The tie designs used by the GPU tie tests: the oracle's selection on
-    them is the one derived by hand from the lower-id rule (page-4 write-up,
+    them is the one derived by hand from the lower-id rule (GLM-5.2 write-up,
     'How it works (validated core mechanics)'), and the gate weights are
     exactly rsf / k (every selected affinity is 1/2)."""
     from helpers import tie_design
