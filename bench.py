@@ -60,7 +60,7 @@ LAYER_KERNEL_SOURCES = ("quantized_expert_ffn_sigmoid_gb300/csrc/decode.cu",
                         "quantized_expert_ffn_sigmoid_gb300/csrc/select_cta.cuh",
                         "quantized_expert_ffn_sigmoid_gb300/csrc/gemv_common.cuh",
                         "quantized_expert_ffn_sigmoid_gb300/csrc/colimoe_internal.cuh")
-LAYER_KERNEL_TRAFFIC = {"bytes": 178367744, "sources_sha256": "6a433e5773a1d0fa400d20588515ad98cbba9a937b8a56ed3df9ec7a9740134a"}
+LAYER_KERNEL_TRAFFIC = {"bytes": 178367744, "sources_sha256": "31eefbaf7cb71ffae1c8110737a05d84d735aa3cdd5db4105cf5ceb3d781dcf3"}
 WORKLOAD = ("glm_decode_b1: GLM-5.2-shaped MoE layer (H 6144, E 256 in 8 groups, topk_group 4, top-8, "
             "moe_inter 2048, 1 shared expert, int4 per-row scales, rsf 2.5), decode batch 1, "
             "1000 independent seeded positions per step, one layer call each")

@@ -19,11 +19,12 @@
 //             in order in shared memory) and publishes each as one 64-bit
 //             word (value, call tag); every CTA polls the E words, then runs
 //             the CTA-wide selection itself (identical in every CTA), so no
-//             grid barrier and no separate router launch are needed.  Only
-//             the router's weights are read before the logits are out; the
-//             shared expert's tiles (the first items of the first CTAs) are
-//             then prefetched into L2 only, so that no shared-memory slot waits
-//             on them while the routing completes.
+//             grid barrier and no separate router launch are needed.  Before
+//             the dependency wait a CTA whose first item is a shared-expert
+//             tile (known without the routing) requests that tile's rows, and
+//             it computes the tile's h while the logits are exchanged and the
+//             selection runs (with group scales, whose scale slots share the
+//             router's scratch, the tile is only prefetched into L2).
 // Phases:
 //   1. gate/up: the 32-row tiles of every selected expert (shared first) are
 //      dealt round-robin to the CTAs; each warp streams its row pairs with
