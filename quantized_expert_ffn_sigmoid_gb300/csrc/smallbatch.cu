@@ -297,16 +297,21 @@ __global__ void __launch_bounds__(SB_THREADS, 1) sb_gemm(const __grid_constant__
       if (t_item[mid] <= it) lo = mid; else hi = mid - 1;
     }
     SbItem d;
-    const int cnt = t_cnt[lo], ntg = (cnt + cap - 1) / cap;
-    const int li = it - t_item[lo];
-    d.tile = li / ntg;
-    const int tg = li % ntg;
-    d.ntok = min(cap, cnt - tg * cap);
-    d.pair0 = t_off[lo] + tg * cap;
+    const int cnt = t_cnt[lo];
     const int e = t_exp[lo];
     d.shared = e >= E;
     d.ex = d.shared ? e - E : ep_local_mul(P.ep_mul, e);
     d.inter = d.shared ? c.shared_inter : c.inter;
+    // an entry's items run position group by position group, each over all
+    // its tiles: the CTAs that take a hot tile's later groups find its rows
+    // in L2 (read by the first group a fraction of a round earlier) instead
+    // of all reading them from HBM at the same time
+    const int ntiles = GU ? d.inter / RA : H / SB_ROWS;
+    const int li = it - t_item[lo];
+    d.tile = li % ntiles;
+    const int tg = li / ntiles;
+    d.ntok = min(cap, cnt - tg * cap);
+    d.pair0 = t_off[lo] + tg * cap;
     d.chunks = (GU ? H : d.inter) / ck;
     return d;
   };
