@@ -60,6 +60,13 @@ def test_host_only_entry_points(lib):
     offs = [L.status, L.n_entries, L.entry_expert, L.qx, L.dx, L.qh, L.dh, L.o]
     assert all(o % 16 == 0 for o in offs) and L.o < L.total
     assert cm.coli_moe_strerror(cm.COLI_EWORKSPACE) == "workspace too small"
+    # the header cleared by coli_moe_workspace_init (status block, device
+    # counters, router exchange words) is the size the header file states,
+    # and the tables start after it
+    import re
+    doc = open(os.path.join(ROOT, "include", "coli_moe.h")).read()
+    cleared = int(re.search(r"min\(ws_bytes, (\d+)\) bytes", doc).group(1))
+    assert L.status == 0 and cleared <= L.n_entries
     bad = cm.Cfg.of(synth.GLM)
     bad.hidden = 100
     assert cm.coli_moe_workspace_size(bad, 4) == 0
