@@ -183,7 +183,12 @@ int coli_moe_route(const coli_moe_cfg* cfg, const float* x, int32_t T,
 int coli_moe_quantize_act(const float* x, int32_t T, int32_t K,
                           int8_t* q, float* d, cudaStream_t stream);
 
-/* The expert layer for given routing: quantise x, build the batch-union
+/* The expert layer for given routing (colibrì v1.0 README, "What's
+ * implemented": Q8_0-style int8 activations against packed int4 / int8
+ * weights, batch-union MoE, the always-on shared expert; "Experimental Metal
+ * backend": the routed-expert SwiGLU; the combine weights are the router's, as
+ * "How it works (validated core mechanics)" of the GLM-5.2 write-up gives
+ * them): quantise x, build the batch-union
  * tables, run each distinct expert once over its positions (gate/up, SwiGLU,
  * re-quantise h, down) and combine
  *     y[t] = sum_j topk_w[t][j] * o[t,j] + sum_s o_shared_s[t]
@@ -197,10 +202,11 @@ int coli_moe_forward(const coli_moe_cfg* cfg, const coli_moe_weights* weights,
                      const int32_t* topk_idx, const float* topk_w, float* y,
                      void* ws, size_t ws_bytes, cudaStream_t stream);
 
-/* The whole layer: coli_moe_route followed by coli_moe_forward, with the
+/* The whole layer (the router and the expert layer above, with the passages
+ * they cite): coli_moe_route followed by coli_moe_forward, with the
  * same arguments, results and status rules as the two calls (topk_idx and
  * topk_w are outputs here, and the forward part reads them).  For a single
- * position (T == 1, packed int4) that fits the fused kernel's shared memory,
+ * position (T == 1, packed int4 or int2) that fits the fused kernel's shared memory,
  * the router runs inside the expert-layer kernel: one launch per call, the
  * shared expert's gate/up rows requested before the routing is known.  The
  * results are bit-identical to the two separate calls. */
@@ -211,7 +217,7 @@ int coli_moe_layer(const coli_moe_cfg* cfg, const coli_moe_weights* weights,
                    void* ws, size_t ws_bytes, cudaStream_t stream);
 
 /* The two launches coli_moe_forward makes, callable separately (e.g. to time
- * the expert kernel alone).  coli_moe_dispatch quantises x and builds the
+ * the expert kernel alone; the operations and passages of coli_moe_forward).  coli_moe_dispatch quantises x and builds the
  * union tables in ws; coli_moe_experts runs the expert products and the
  * combine from those tables.  Same arguments and rules as coli_moe_forward;
  * coli_moe_experts must follow a coli_moe_dispatch with the same T on the
