@@ -598,7 +598,7 @@ cudaError_t launch_one(const SbMaps& maps, const SbArgs& A, size_t smem, int gri
 template <int BITS, bool GS>
 cudaError_t run_sb(const ExpertParams& P, int n_sm, cudaStream_t st, bool dump, int max_pairs) {
   const coli_moe_cfg& c = P.cfg;
-  const int H = c.hidden, E = c.n_experts, I = c.inter, Is = c.shared_inter, ns = c.n_shared;
+  const int H = c.hidden, I = c.inter, Is = c.shared_inter, ns = c.n_shared;
   SbPlan pg, pd;
   if (!sb_plan(c, P.L, true, &pg) || !sb_plan(c, P.L, false, &pd)) return cudaErrorInvalidValue;
   const size_t rb_h = (size_t)H * BITS / 8;
